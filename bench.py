@@ -1,0 +1,400 @@
+"""Benchmark of the sparse-decode path on one or more GB300s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch: write the step's new
+tokens into the caches, cast the queries the writer emits as e4m3, row
+lengths, index scores, top-k with the emitted sparse table, attention (split-K
++ merge).  The workload is one of the five seeded synthetic configurations
+(default 2: 32 fp8 sequences of 4096..8192 tokens, 16 query heads per KV
+head, top-128 pages).
+
+Timing: every step is bracketed by CUDA events on the launching stream; an L2
+flush (a 256 MiB memset, twice the L2) runs before each step and is not
+timed; the reported ms_per_step is the mean of the K event intervals, max over
+ranks.  The index-score and attention kernels are timed by events inside the
+step for the roofline.  SM clocks are sampled with nvidia-smi during the timed
+region.  `e2e` repeats the measurement through the public step API with the
+step's inputs copied from pinned host memory and the attention output copied
+back, inside the timed region.  `cpu_baseline` times the CPU oracle (C, OpenMP)
+on a bounded sample of the same workload; `--impl reference` reports that
+oracle as the reference arm.
+
+Under torchrun each rank runs its own batch (its own seeds) on its own GPU:
+weak scaling, no collective on the data path.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_FALLBACK_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "block_sparse_paged_score_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, files):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    want = kernel_source_hash(files)
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[2] == want:
+            return float(f[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def workload_desc(w):
+    lens = w.decode_lens
+    d = {"workload": w.name, "decode_seqs": int(w.num_decode), "q_len": int(w.q_len),
+         "context_min": int(lens.min()) if len(lens) else 0, "context_max": int(lens.max()) if len(lens) else 0,
+         "kv_heads": w.hkv, "q_heads_per_kv": w.group, "top_k_pages": w.k_pages, "page_tokens": 16,
+         "block_tokens": 128, "kv_dtype": ["bf16", "fp8_e4m3", "mxfp4"][w.kv_dtype],
+         "index_dtype": ["bf16", "fp8_e4m3", "mxfp4"][w.idx_dtype]}
+    if w.prefill_chunks:
+        d["prefill_chunks"] = [list(c) for c in w.prefill_chunks]
+        d["pad_rows"] = int(w.num_pad_tokens)
+    d["l2"] = "flushed before every step (256 MiB memset, excluded from the step time)"
+    return d
+
+
+def index_algorithmic_bytes(w, rows_scored=None):
+    """Bytes the decode index scorer must move at minimum: every cached index
+    key of every scored sequence once, the index queries, and the score rows."""
+    per_tok = {0: 256, 1: 132, 2: 68}[w.idx_dtype]
+    L = w.decode_lens.astype(np.int64)
+    keys = int(L.sum()) * per_tok * w.hidx
+    q = w.num_decode_tokens * w.hidx * 128 * (2 if w.idx_q_dtype == 0 else 1)
+    scores = w.num_decode_rows * w.max_pages * 4
+    return keys + q + scores
+
+
+def attention_algorithmic_bytes(w, ctx_total):
+    """Selected K+V bytes once per row, the queries and the bf16 output."""
+    per_tok = {0: 512, 1: 256, 2: 136}[w.kv_dtype]
+    q = w.num_decode_tokens * w.hq * 128 * (2 if w.q_dtype == 0 else 1)
+    out = w.num_decode_tokens * w.hq * 128 * 2
+    return int(ctx_total) * per_tok + q + out
+
+
+# ---------------------------------------------------------------------------
+class OracleStep:
+    """The CPU oracle's step on the first `n` decode sequences of the batch:
+    write of their new tokens, e4m3 casts, scores, top-k, attention.  Their
+    caches are written once, outside the timing."""
+
+    def __init__(self, w, n):
+        import oracle as O
+        self.O, self.w = O, w
+        seqs = list(range(n))
+        self.kv = np.zeros(w.num_blocks * O.kv_block_bytes(w.kv_dtype, w.hkv), np.uint8)
+        self.idx = np.zeros(w.num_blocks * w.hidx * O.index_field_bytes(w.idx_dtype), np.uint8)
+        for k, v, ik, slot in w.context_batches(seqs=seqs):
+            O.kv_page_write(w.kv_dtype, w.hkv, self.kv, w.k_scale, w.v_scale, w.idx_dtype, w.hidx, self.idx,
+                            k, v, ik, slot)
+        self.q, self.iq = w.queries()
+        self.rs, self.rl = O.row_lengths_decode(w.decode_lens, w.q_len, w.hkv)
+        self.rows = np.array([(s * w.q_len + j) * w.hkv + h for s in seqs for j in range(w.q_len)
+                              for h in range(w.hkv)], np.int32)
+        k, v, ik, slot = w.step_tokens()
+        keep = np.array([i for i, (s, _) in enumerate(w.step_token_positions()) if s < n], np.int64)
+        self.new = (k[keep], v[keep], ik[keep], slot[keep])
+        self.tokens = n * w.q_len
+        self.desc = f"{n} of {w.num_decode} decode sequences ({self.tokens} query tokens) per step"
+
+    def run(self):
+        O, w = self.O, self.w
+        k, v, ik, slot = self.new
+        t0 = time.perf_counter()
+        O.kv_page_write(w.kv_dtype, w.hkv, self.kv, w.k_scale, w.v_scale, w.idx_dtype, w.hidx, self.idx, k, v, ik,
+                        slot)
+        qd = self.q if w.q_dtype == 0 else O.cast_e4m3(self.q)
+        iqd = self.iq if w.idx_q_dtype == 0 else O.cast_e4m3(self.iq)
+        sc = O.index_score(w.idx_dtype, w.hidx, self.idx, iqd, w.idx_q_dtype, w.block_table, self.rs, self.rl,
+                           w.max_pages, rows=self.rows)
+        ti, sb, ctx = O.topk_select(sc, self.rs, self.rl, w.block_table, 1 if w.kv_dtype == 2 else 0, w.k_pages,
+                                    True, rows=self.rows)
+        O.sparse_attention(w.kv_dtype, w.hkv, self.kv, w.k_scale, w.v_scale, qd, w.q_dtype, w.group, sb, ctx,
+                           w.sm_scale, rows=self.rows)
+        return time.perf_counter() - t0
+
+
+def oracle_sample(w, seconds):
+    """An OracleStep whose run takes about `seconds` (at least one sequence)."""
+    one = OracleStep(w, 1)
+    t1 = min(one.run() for _ in range(2))
+    n = int(max(1, min(w.num_decode, seconds / max(t1, 1e-6))))
+    return one if n == 1 else OracleStep(w, n)
+
+
+def cpu_oracle_rate(w, seconds=12.0):
+    import oracle as O
+    o = oracle_sample(w, seconds)
+    dt = o.run()
+    return o.tokens / dt, O.num_threads(), o.desc + ", one pass"
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as O
+    from block_sparse_paged_score_gb300 import workloads as W
+
+    w = W.workload(args.config)
+    # each step a bounded sample of the batch, sized so that the whole run ends within a few minutes
+    o = oracle_sample(w, max(0.005, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        o.run()
+    times = [o.run() for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    value = o.tokens / (ms / 1e3)
+    line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_desc(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
+                             "sample": o.desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+
+    from block_sparse_paged_score_gb300 import bsp, step, workloads as W
+
+    bsp.lib()
+    spec = dict(W.CONFIGS[args.config])
+    spec["seed"] = spec["seed"] + 1000 * rank  # each rank its own batch
+    w = W.Workload(spec)
+
+    def t(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    kv = bsp.KvCache(w.kv_dtype, w.hkv, w.num_blocks, w.k_scale, w.v_scale, device=dev)
+    idx = bsp.IndexCache(w.idx_dtype, w.hidx, w.num_blocks, device=dev)
+    for k, v, ik, slot in w.context_batches():
+        bsp.kv_page_write(kv, idx, t(k), t(v), t(ik), t(slot))
+    bt = t(w.block_table)
+    k, v, ik, slot = w.step_tokens()
+    q, iq = w.queries()
+    mixed = bool(w.prefill_chunks)
+    if mixed:
+        st = step.MixedStep(w, kv, idx, bt, device=dev)
+    else:
+        st = step.DecodeStep(w, kv, idx, bt, device=dev)
+    inputs = {"k": t(k), "v": t(v), "idx_k": t(ik), "slot": t(slot), "q": t(q), "idx_q": t(iq),
+              "seq_lens": t(w.decode_lens)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    K, Wm = args.steps, args.warmup
+    nev = 5
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
+    for evs in events:  # create the CUDA events before the timed region
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    def one(evs=None):
+        flush.zero_()
+        st.run(inputs["k"], inputs["v"], inputs["idx_k"], inputs["slot"], inputs["q"], inputs["idx_q"],
+               inputs["seq_lens"], events=evs, stream=stream)
+
+    for _ in range(Wm):
+        one()
+    torch.cuda.synchronize()
+    st.dev_err.zero_()
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)  # let nvidia-smi take a first sample
+    launches0 = bsp.launch_count()
+    for i in range(K):
+        one(events[i])
+    torch.cuda.synchronize()
+    launches = bsp.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    err = int(st.dev_err.item())
+    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(K)]
+    score_ms = [events[i][1].elapsed_time(events[i][2]) for i in range(K)]
+    attn_ms = [events[i][3].elapsed_time(events[i][4]) for i in range(K)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    tokens = w.num_decode_tokens + (w.num_prefill_tokens if mixed else 0)
+    value = tokens * world / (ms / 1e3)
+
+    # roofline of the dominant kernel (the index scorer streams the most bytes)
+    peak, peak_kind = measured_peaks()
+    score_bytes = index_algorithmic_bytes(w)
+    ctx_total = int(st.sparse_ctx[:w.num_decode_rows].sum().item())
+    attn_bytes = attention_algorithmic_bytes(w, ctx_total)
+    score_s = statistics.mean(score_ms) / 1e3
+    attn_s = statistics.mean(attn_ms) / 1e3
+    roof = {"kernel": "index_score (decode)", "bound": "hbm", "achieved": score_bytes / score_s / 1e9,
+            "peak": peak, "unit": "GB/s", "frac": score_bytes / score_s / 1e9 / peak,
+            "traffic": recorded_traffic("index_score_kernel", w.name, ["index_score.cu", "common.cuh"]),
+            "algorithmic_bytes": score_bytes, "us_per_launch": score_s * 1e6, "peak_source": peak_kind}
+    kernels = {"sparse_pa_decode+merge": {"achieved_gbs": attn_bytes / attn_s / 1e9,
+                                          "frac": attn_bytes / attn_s / 1e9 / peak,
+                                          "algorithmic_bytes": attn_bytes, "us_per_step": attn_s * 1e6}}
+
+    # end to end through the public step API, inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        host = {kk: vv.cpu() for kk, vv in inputs.items()}
+        hs = step.HostDecodeStep(st, host, device=dev)
+        Ke = min(K, 500)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+        for _ in range(3):
+            flush.zero_()
+            hs.run(stream)
+        torch.cuda.synchronize()
+        for i in range(Ke):
+            flush.zero_()
+            ev[i][0].record(stream)
+            hs.run(stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": hs.h2d_bytes, "d2h_bytes_per_step": hs.d2h_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, threads, desc = cpu_oracle_rate(w)
+        cpu = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "e4m3" if w.kv_dtype == 1 else ("mxfp4" if w.kv_dtype == 2 else "bf16"),
+                "data": "synthetic", "config": workload_desc(w), "roofline": roof, "kernels": kernels,
+                "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
+                "device_errors": err}
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

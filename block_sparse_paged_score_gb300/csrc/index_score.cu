@@ -1,0 +1,286 @@
+// index_score.cu -- a2: page scores of the index query against the index-key
+// cache (ROCm/ATOM PR 2962, commit "... page-128 block table": fp32 scores of
+// each row over its context, -inf where nothing is scored; "Known limits":
+// the scorer runs at the score workspace's full width).
+//
+//   scores[r, p] = max_{t in page p, t < L_r} sum_d q[r, d] * k[t, d]
+//   scores[r, p] = -inf for p >= ceil(L_r / 16)
+//
+// Work unit: one CTA per (query group, index head, chunk of 128-token
+// blocks).  A query group is q_group consecutive tokens of one sequence (the
+// decode query length), so the index cache of a sequence is read once per
+// group.  Thread 0 streams whole index fields (16896 B fp8, 32768 B bf16,
+// 8704 B MXFP4 per block and head) into a shared-memory ring with 1-D TMA
+// bulk copies completing on mbarriers; the four warps each score 32 tokens of
+// a block (two 16-token pages) on the tensor cores:
+//   A = 16 keys x 16 dims (fp8 -> f16 exactly, e2m1 -> f16 exactly, or bf16),
+//   B = 16 dims x 8 query rows (the group's rows; unused columns are zero),
+//   C = fp32.
+// The dims of each mma are a permutation of 16 real dims chosen so that every
+// thread reads 16-byte (or 4-byte) runs of a key row; A and B use the same
+// permutation, so each dot product is unchanged.  The per-token fp8 scale and
+// the per-32-dim e8m0 scales are applied to the fp32 partial sums, then the
+// page max is a shuffle reduction over the 16 tokens of the tile.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsp {
+
+namespace {
+
+template <int KEY>
+struct KeyFmt;
+template <>
+struct KeyFmt<BSP_BF16> {
+  static constexpr int kField = kBf16IndexField;
+  static constexpr int kStages = 3;
+};
+template <>
+struct KeyFmt<BSP_FP8_E4M3> {
+  static constexpr int kField = kFp8IndexField;
+  static constexpr int kStages = 4;
+};
+template <>
+struct KeyFmt<BSP_MXFP4> {
+  static constexpr int kField = kMxField;
+  static constexpr int kStages = 6;
+};
+
+template <int KEY>
+constexpr int smem_bytes() {
+  return KeyFmt<KEY>::kStages * KeyFmt<KEY>::kField + KeyFmt<KEY>::kStages * 8;
+}
+
+// first of the four real dims that B fragment m of thread t covers
+template <int KEY>
+__device__ __forceinline__ int frag_dim(int m, int t) {
+  if (KEY == BSP_FP8_E4M3) return 16 * (t + 4 * (m >> 2)) + 4 * (m & 3);
+  if (KEY == BSP_MXFP4) return 32 * (m >> 1) + 8 * t + 4 * (m & 1);
+  return 8 * (t + 4 * (m >> 1)) + 4 * (m & 1);
+}
+
+__device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off, float (&v)[4]) {
+  if (q_dtype == BSP_BF16) {
+    const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(q) + off);
+    v[0] = bf16_bits_to_float(w.x & 0xFFFF);
+    v[1] = bf16_bits_to_float(w.x >> 16);
+    v[2] = bf16_bits_to_float(w.y & 0xFFFF);
+    v[3] = bf16_bits_to_float(w.y >> 16);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(q) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = e4m3_to_float(w >> (8 * i));
+  }
+}
+
+template <int KEY>
+__global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
+  constexpr int FB = KeyFmt<KEY>::kField;
+  constexpr int S = KeyFmt<KEY>::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * FB);
+  __shared__ int s_len[8], s_row[8], s_seq;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int group = blockIdx.x / p.hidx, h = blockIdx.x % p.hidx;
+  const int chunk = blockIdx.y;
+  const int tok0 = group * p.q_group;
+  const int ntok = min(p.q_group, p.num_tokens - tok0);
+  const int max_len = p.max_pages * kPage;
+
+  if (tid < 8) {
+    int L = 0, r = -1;
+    if (tid < ntok) {
+      r = (tok0 + tid) * p.hidx + h;
+      L = min(max(p.row_len[r], 0), max_len);
+      if (p.row_seq[r] != p.row_seq[tok0 * p.hidx + h]) set_err(p.err, BSP_DEVERR_GROUP_SEQ);
+    }
+    s_len[tid] = L;
+    s_row[tid] = r;
+  }
+  if (tid == 0) {
+    s_seq = p.row_seq[tok0 * p.hidx + h];
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  int lmax = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) lmax = max(lmax, s_len[i]);
+  const int seq = s_seq;
+  const int blk0 = chunk * p.blocks_per_chunk;
+  const int nb = max(0, min(p.blocks_per_chunk, (lmax + kBlock - 1) / kBlock - blk0));
+  const int page_end = min((blk0 + p.blocks_per_chunk) * kPagesPerSide, p.max_pages);
+
+  // pages of this chunk past every row's context: -inf
+  {
+    const int pfirst = (blk0 + nb) * kPagesPerSide;
+    const int npg = max(0, page_end - pfirst);
+    for (int i = tid; i < ntok * npg; i += blockDim.x)
+      p.scores[static_cast<int64_t>(s_row[i / npg]) * p.max_pages + pfirst + i % npg] = -INFINITY;
+  }
+  if (nb == 0) return;
+
+  auto issue = [&](int i) {
+    int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + i];
+    if (bid < 0 || bid >= p.num_blocks) {
+      set_err(p.err, BSP_DEVERR_BLOCK_ID);
+      bid = 0;
+    }
+    const int st = i % S;
+    mbar_arrive_expect_tx(&bars[st], FB);
+    bulk_g2s(smem + st * FB, p.idx_base + static_cast<int64_t>(bid) * p.block_stride + static_cast<int64_t>(h) * FB,
+             FB, &bars[st]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < min(S, nb); ++i) issue(i);
+
+  // B fragments: query row g of the group (zero beyond the group)
+  uint32_t qb[8][2];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (g < ntok) load_q4(p.q, p.q_dtype, (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim + frag_dim<KEY>(m, t), v);
+    if (KEY == BSP_BF16) {
+      qb[m][0] = pack_bf16x2(v[0], v[1]);
+      qb[m][1] = pack_bf16x2(v[2], v[3]);
+    } else {
+      qb[m][0] = pack_f16x2(v[0], v[1]);
+      qb[m][1] = pack_f16x2(v[2], v[3]);
+    }
+  }
+  const int len_lo = s_len[min(2 * t, 7)], len_hi = s_len[min(2 * t + 1, 7)];
+
+  for (int i = 0; i < nb; ++i) {
+    const int st = i % S;
+    mbar_wait(&bars[st], (i / S) & 1, p.err);
+    const uint32_t sbase = smem_u32(smem + st * FB);
+    const int blk_pos = (blk0 + i) * kBlock;
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile) {
+      const int tokb = 32 * warp + 16 * tile;
+      float v0, v1, v2, v3;
+      if (KEY == BSP_FP8_E4M3) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ra_row = sbase + (tokb + g) * 128, rb_row = ra_row + 8 * 128;
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii) {
+          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2_scaled(wa[j], a0, a2);
+            e4m3x4_to_f16x2_scaled(wb[j], a1, a3);
+            mma_f16(acc, a0, a1, a2, a3, qb[4 * ii + j][0], qb[4 * ii + j][1]);
+          }
+        }
+        // per-token scale; the f16 keys hold value * 2^-8
+        const float sg = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g) * 4) * 256.f;
+        const float sg8 =
+            *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g + 8) * 4) * 256.f;
+        v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
+      } else if (KEY == BSP_MXFP4) {
+        float acc[4][4];
+#pragma unroll
+        for (int G = 0; G < 4; ++G) acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+        const uint32_t ra_row = sbase + (tokb + g) * 64, rb_row = ra_row + 8 * 64;
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          const uint32_t wa = lds32(ra_row + 16 * G + 4 * t), wb = lds32(rb_row + 16 * G + 4 * t);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t a0 = e2m1x2_to_f16x2((wa >> (16 * hh)) & 0xFF);
+            const uint32_t a2 = e2m1x2_to_f16x2((wa >> (16 * hh + 8)) & 0xFF);
+            const uint32_t a1 = e2m1x2_to_f16x2((wb >> (16 * hh)) & 0xFF);
+            const uint32_t a3 = e2m1x2_to_f16x2((wb >> (16 * hh + 8)) & 0xFF);
+            mma_f16(acc[G], a0, a1, a2, a3, qb[2 * G + hh][0], qb[2 * G + hh][1]);
+          }
+        }
+        const uint32_t sa = lds32(sbase + kMxScaleOff + (tokb + g) * 4);
+        const uint32_t sb = lds32(sbase + kMxScaleOff + (tokb + g + 8) * 4);
+        v0 = v1 = v2 = v3 = 0.f;
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          const float ca = e8m0_to_float((sa >> (8 * G)) & 0xFF), cb = e8m0_to_float((sb >> (8 * G)) & 0xFF);
+          v0 = fmaf(acc[G][0], ca, v0);
+          v1 = fmaf(acc[G][1], ca, v1);
+          v2 = fmaf(acc[G][2], cb, v2);
+          v3 = fmaf(acc[G][3], cb, v3);
+        }
+      } else {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ra_row = sbase + (tokb + g) * 256, rb_row = ra_row + 8 * 256;
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+          mma_bf16(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
+          mma_bf16(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
+        }
+        v0 = acc[0], v1 = acc[1], v2 = acc[2], v3 = acc[3];
+      }
+      // mask tokens past each row's length, then the page max over 16 tokens
+      const int pos = blk_pos + tokb + g;
+      float m_lo = fmaxf(pos < len_lo ? v0 : -INFINITY, pos + 8 < len_lo ? v2 : -INFINITY);
+      float m_hi = fmaxf(pos < len_hi ? v1 : -INFINITY, pos + 8 < len_hi ? v3 : -INFINITY);
+#pragma unroll
+      for (int m = 4; m < 32; m <<= 1) {
+        m_lo = fmaxf(m_lo, __shfl_xor_sync(0xffffffffu, m_lo, m));
+        m_hi = fmaxf(m_hi, __shfl_xor_sync(0xffffffffu, m_hi, m));
+      }
+      const int page = (blk0 + i) * kPagesPerSide + 2 * warp + tile;
+      if (g == 0 && page < p.max_pages) {
+        if (2 * t < ntok)
+          p.scores[static_cast<int64_t>(s_row[2 * t]) * p.max_pages + page] =
+              page < (len_lo + kPage - 1) / kPage ? m_lo : -INFINITY;
+        if (2 * t + 1 < ntok)
+          p.scores[static_cast<int64_t>(s_row[2 * t + 1]) * p.max_pages + page] =
+              page < (len_hi + kPage - 1) / kPage ? m_hi : -INFINITY;
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && i + S < nb) {
+      fence_proxy_async();
+      issue(i + S);
+    }
+  }
+}
+
+template <int KEY>
+cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
+  constexpr int bytes = smem_bytes<KEY>();
+  static bool configured = false;  // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  index_score_kernel<KEY><<<grid, 128, bytes, s>>>(p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) {
+  if (p.num_rows == 0 || p.max_pages == 0) return cudaSuccess;
+  p.num_groups = (p.num_tokens + p.q_group - 1) / p.q_group;
+  const int64_t max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+  // about four CTAs per SM of streaming work, 2..32 blocks per CTA
+  int64_t cb = (static_cast<int64_t>(p.num_groups) * p.hidx * max_blocks + 4 * num_sms - 1) / (4 * num_sms);
+  cb = cb < 2 ? 2 : (cb > 32 ? 32 : cb);
+  p.blocks_per_chunk = static_cast<int32_t>(cb);
+  const dim3 grid(static_cast<unsigned>(p.num_groups * p.hidx), static_cast<unsigned>((max_blocks + cb - 1) / cb));
+  switch (p.idx_dtype) {
+    case BSP_BF16:
+      return launch_key<BSP_BF16>(p, grid, s);
+    case BSP_FP8_E4M3:
+      return launch_key<BSP_FP8_E4M3>(p, grid, s);
+    default:
+      return launch_key<BSP_MXFP4>(p, grid, s);
+  }
+}
+
+}  // namespace bsp

@@ -1,0 +1,360 @@
+// index_score_prefill_tc.cu -- a2': index scores of prefill chunks as a dense
+// fp8 contraction on the 5th-generation tensor cores (ROCm/ATOM PR 2962,
+// commit "... page-128 block table": the prefill scorer; its scores are laid
+// out as the decode scorer's, so selection and emission are shared).
+//
+//   S[i, t] = s_t * sum_d q[i, d] * k8[t, d]      (e4m3 x e4m3, fp32 accumulate)
+//   scores[i, p] = max_{t in page p, t < L_i} S[i, t],  -inf past ceil(L_i/16)
+//
+// One CTA = one tile of 128 consecutive query rows of one chunk (a chunk is
+// a run of query tokens of one sequence) x a range of 16 key blocks (2048
+// keys).  Warp 0, lane 0 is the producer and the MMA issuer:
+//   - the query tile and each pair of key blocks arrive by 2-D TMA tensor
+//     loads with 128-byte swizzle (box 128 rows x 128 B) on mbarriers; key
+//     rows of block b start at row b * (block_stride / 128) of the index
+//     cache seen as a [rows, 128 B] tensor; a missing block loads from an
+//     out-of-range row and is zero-filled;
+//   - tcgen05.mma.cta_group::1.kind::f8f6f4, M = 128 queries, N = 256 keys,
+//     K = 4 x 32 dims, into one of two 256-column fp32 TMEM accumulators;
+//     tcgen05.commit releases the key stage and signals the accumulator.
+// Warps 1..8 are the epilogue: warp w reads TMEM lanes 32*(w%4).. (its
+// quarter) and half of the 256 columns with tcgen05.ld, multiplies by the
+// per-token fp32 scales (staged in shared memory per tile), masks keys at
+// or past the row's causal length, max-pools 16 keys into a page score and
+// stores 8 pages per row per tile.  Accumulator double-buffering lets the
+// MMAs of the next tile run under the epilogue of this one.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsp {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kKeyBlocksPerCta = 16;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (1 + kEpiWarps);
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 B
+constexpr int kSmemBytes = 1024 /*align slack*/ + kTileBytes /*A*/ + kStages * 2 * kTileBytes /*B*/ +
+                           2 * 256 * 4 /*scales*/ + 16 * 8 /*barriers*/ + 16;
+
+struct SmemLayout {
+  uint8_t* a;
+  uint8_t* b;  // [stage][256 rows][128 B]
+  float* scales;  // [2][256]
+  uint64_t* bars;  // a_full, b_full[S], b_empty[S], acc_full[2], acc_empty[2]
+  uint32_t* tmem_slot;
+};
+
+__device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
+  SmemLayout L;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  L.a = base;
+  L.b = base + kTileBytes;
+  L.scales = reinterpret_cast<float*>(L.b + kStages * 2 * kTileBytes);
+  L.bars = reinterpret_cast<uint64_t*>(L.scales + 2 * 256);
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 16);
+  return L;
+}
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 B apart (SBO), leading offset unused for a swizzled K-major operand.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                  // SWIZZLE_128B
+  return d;
+}
+
+// instruction descriptor: kind::f8f6f4, D fp32, A = B = e4m3, both K-major,
+// N = 256, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void epi_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    index_score_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                               PrefillScoreParams p, int32_t oob_row) {
+  extern __shared__ uint8_t smem_raw[];
+  const SmemLayout sm = carve(smem_raw);
+  uint64_t* a_full = sm.bars;
+  uint64_t* b_full = sm.bars + 1;
+  uint64_t* b_empty = sm.bars + 1 + kStages;
+  uint64_t* acc_full = sm.bars + 1 + 2 * kStages;
+  uint64_t* acc_empty = sm.bars + 3 + 2 * kStages;
+  __shared__ int s_tok0, s_tok1, s_lmax, s_seq;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kb0 = blockIdx.y * kKeyBlocksPerCta;
+  const int rows_per_block = static_cast<int>(p.block_stride / 128);
+
+  if (tid == 0) {
+    // locate this tile: chunks in order, ceil(size/128) tiles each
+    int t = blockIdx.x, tok0 = -1, tok1 = -1;
+    for (int c = 0; c < p.num_chunks; ++c) {
+      const int a = p.cu_tokens[c], b = p.cu_tokens[c + 1];
+      const int nt = (b - a + 127) / 128;
+      if (t < nt) {
+        tok0 = a + 128 * t;
+        tok1 = min(b, tok0 + 128);
+        break;
+      }
+      t -= nt;
+    }
+    s_tok0 = tok0;
+    s_tok1 = tok1;
+    s_lmax = 0;
+    s_seq = tok0 >= 0 ? p.row_seq[tok0] : 0;
+    mbar_init(a_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 32 * kEpiWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int tok0 = s_tok0, tok1 = s_tok1;
+  if (tok0 < 0) return;  // past the last tile (the grid is an upper bound)
+
+  // the epilogue's row and its causal length; the tile's longest row
+  const int quarter = warp & 3;
+  const int row = 32 * quarter + lane;
+  const int tok = tok0 + row;
+  const bool row_ok = warp >= 1 && tok < tok1;
+  const int max_len = p.max_pages * kPage;
+  int L = 0;
+  if (row_ok) {
+    L = min(max(p.row_len[tok], 0), max_len);
+    if (p.row_seq[tok] != s_seq) set_err(p.err, BSP_DEVERR_GROUP_SEQ);
+    if (warp <= 4) atomicMax(&s_lmax, L);
+  }
+  __syncthreads();
+  const int nb = max(0, min(kKeyBlocksPerCta, (s_lmax + kBlock - 1) / kBlock - kb0));
+  const int ntiles = (nb + 1) / 2;
+  const int page_end = min((kb0 + kKeyBlocksPerCta) * kPagesPerSide, p.max_pages);
+  const int seq = s_seq;
+
+  if (ntiles == 0) {
+    if (row_ok && warp <= 4)
+      for (int pg = kb0 * kPagesPerSide; pg < page_end; ++pg)
+        p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
+    return;
+  }
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(sm.tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *sm.tmem_slot;
+
+  auto block_row = [&](int blk) -> int {
+    if (blk >= kb0 + nb) return oob_row;
+    const int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk];
+    if (bid < 0 || bid >= p.num_blocks) {
+      set_err(p.err, BSP_DEVERR_BLOCK_ID);
+      return oob_row;
+    }
+    return bid * rows_per_block;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      auto load_b = [&](int j) {
+        const int st = j % kStages;
+        mbar_arrive_expect_tx(&b_full[st], 2 * kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          tma_load_2d(sm.b + (st * 2 + h) * kTileBytes, &tmap_k, 0, block_row(kb0 + 2 * j + h), &b_full[st]);
+      };
+      mbar_arrive_expect_tx(a_full, kTileBytes);
+      tma_load_2d(sm.a, &tmap_q, 0, tok0, a_full);
+      for (int j = 0; j < min(kStages, ntiles); ++j) load_b(j);
+      mbar_wait(a_full, 0, p.err);
+      const uint32_t a_addr = smem_u32(sm.a);
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j % kStages, buf = j & 1;
+        mbar_wait(&b_full[st], (j / kStages) & 1, p.err);
+        mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t b_addr = smem_u32(sm.b + st * 2 * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma_f8(tmem + buf * 256, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), k > 0);
+        umma_commit(&b_empty[st]);
+        umma_commit(&acc_full[buf]);
+        if (j + kStages < ntiles) {
+          mbar_wait(&b_empty[st], (j / kStages) & 1, p.err);
+          load_b(j + kStages);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    const int et = tid - 32;           // 0..255
+    const int col0 = 128 * ((warp - 1) >> 2);  // this warp's half of the 256 columns
+    for (int j = 0; j < ntiles; ++j) {
+      const int buf = j & 1;
+      // stage the fp32 scales of the tile's 256 keys (the previous user of
+      // this buffer, tile j-2, is finished: every epilogue thread passed the
+      // barrier below for tile j-1)
+      for (int i = et; i < 256; i += 32 * kEpiWarps) {
+        const int blk = kb0 + 2 * j + (i >> 7);
+        float s = 0.f;
+        if (blk < kb0 + nb) {
+          const int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk];
+          if (bid >= 0 && bid < p.num_blocks)
+            s = *reinterpret_cast<const float*>(p.idx_base + static_cast<int64_t>(bid) * p.block_stride +
+                                                kFp8IndexScaleOff + (i & 127) * 4);
+        }
+        sm.scales[buf * 256 + i] = s;
+      }
+      epi_barrier();
+      mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float pv[8];
+      const int key0 = (kb0 + 2 * j) * kBlock;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        const int c0 = col0 + 32 * cc;
+        tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * 256 + c0, v);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int col = c0 + 16 * hh + c;
+            const float x = v[16 * hh + c] * sm.scales[buf * 256 + col];
+            m = key0 + col < L ? fmaxf(m, x) : m;
+          }
+          pv[2 * cc + hh] = m;
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(&acc_empty[buf]);
+      if (row_ok) {
+        const int pg0 = (kb0 + 2 * j) * kPagesPerSide + col0 / kPage;
+        float* dst = p.scores + static_cast<int64_t>(tok) * p.max_pages + pg0;
+        if (pg0 + 8 <= p.max_pages && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+          reinterpret_cast<float4*>(dst)[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+        } else {
+          for (int i = 0; i < 8; ++i)
+            if (pg0 + i < p.max_pages) dst[i] = pv[i];
+        }
+      }
+    }
+    // pages of this key range that no tile covered
+    if (row_ok && warp <= 4)
+      for (int pg = (kb0 + 2 * ntiles) * kPagesPerSide; pg < page_end; ++pg)
+        p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
+  }
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t s) {
+  CUtensorMap tq, tk;
+  const uint64_t key_rows = static_cast<uint64_t>(p.num_blocks) * (p.block_stride / 128);
+  if (!make_map(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map(&tk, p.idx_base, key_rows))
+    return cudaErrorInvalidValue;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(index_score_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+  const dim3 grid(static_cast<unsigned>(p.max_tiles),
+                  static_cast<unsigned>((max_blocks + kKeyBlocksPerCta - 1) / kKeyBlocksPerCta));
+  index_score_prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, p, static_cast<int32_t>(key_rows));
+  return cudaPeekAtLastError();
+}
+
+}  // namespace bsp

@@ -1,0 +1,103 @@
+// kernels.h -- launch parameters and host launchers of the libbsp kernels.
+// Host-side only types; the C ABI in api.cu validates arguments and calls
+// these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsp {
+
+struct KvWriteParams {
+  int32_t kv_dtype, hkv;
+  uint8_t* k_base;
+  uint8_t* v_base;
+  int64_t id_stride, num_blocks;
+  float k_scale, v_scale;
+  int32_t idx_dtype, hidx;  // hidx = 0: no index write
+  uint8_t* idx_base;
+  int64_t idx_block_stride, idx_num_blocks;
+  const uint16_t* k;
+  const uint16_t* v;
+  const uint16_t* idx_k;
+  const int64_t* slot;
+  int32_t num_tokens;
+  int32_t* err;
+};
+cudaError_t launch_kv_page_write(const KvWriteParams& p, cudaStream_t s);
+cudaError_t launch_cast_e4m3(const uint16_t* x, uint8_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_row_lengths_decode(const int32_t* seq_lens, int32_t num_seqs, int32_t q_len, int32_t heads,
+                                      int32_t* row_seq, int32_t* row_len, cudaStream_t s);
+cudaError_t launch_row_lengths_prefill(const int32_t* req, const int32_t* pos, int32_t n, int32_t heads,
+                                       int32_t* row_seq, int32_t* row_len, cudaStream_t s);
+
+struct IndexScoreParams {
+  int32_t idx_dtype, hidx;
+  const uint8_t* idx_base;
+  int64_t block_stride, num_blocks;
+  const void* q;
+  int32_t q_dtype;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* row_seq;
+  const int32_t* row_len;
+  int32_t num_rows, num_tokens, q_group, max_pages;
+  int32_t blocks_per_chunk, num_groups;
+  float* scores;
+  int32_t* err;
+};
+cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s);
+
+struct TopkParams {
+  const float* scores;
+  int32_t num_rows, max_pages;
+  const int32_t* row_seq;
+  const int32_t* row_len;
+  const int32_t* block_table;
+  int32_t bt_stride, id_mul;  // id = block * id_mul + p % 8
+  int32_t k_pages, force_tail;
+  int32_t* topk_idx;
+  int32_t* sparse_bt;
+  int32_t* sparse_ctx;
+};
+cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s);
+
+struct SparsePaParams {
+  int32_t kv_dtype, hkv;
+  const uint8_t* k_base;
+  const uint8_t* v_base;
+  int64_t id_stride, num_ids;
+  float k_scale, v_scale;
+  const void* q;
+  int32_t q_dtype, group;
+  const int32_t* sparse_bt;
+  const int32_t* sparse_ctx;
+  int32_t num_rows, k_pages;
+  float sm_scale;
+  void* out;
+  float* ws;  // partials, nsplit > 1
+  int32_t nsplit, pages_per_split;
+  int32_t* err;
+};
+// split plan shared by the launcher and the workspace query
+void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split);
+size_t sparse_pa_ws_bytes(int32_t num_rows, int32_t nsplit);
+cudaError_t launch_sparse_pa(const SparsePaParams& p, cudaStream_t s, int* launches);
+
+struct PrefillScoreParams {
+  const uint8_t* idx_base;
+  int64_t block_stride, num_blocks;
+  const uint8_t* q;  // e4m3 [tokens, 128]
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* row_seq;
+  const int32_t* row_len;
+  int32_t num_rows;
+  const int32_t* cu_tokens;
+  int32_t num_chunks, max_tiles, max_pages;
+  float* scores;
+  int32_t* err;
+};
+cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t s);
+
+}  // namespace bsp

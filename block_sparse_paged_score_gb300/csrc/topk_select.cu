@@ -1,0 +1,214 @@
+// topk_select.cu -- a3: per-row top-k of 16-token pages and the emitted
+// sparse block table (ROCm/ATOM PR 2962: selection per row,
+// _emit_sparse_block_table_row with pages_per_block 8 or 1, the B12 clamp, "the
+// tail page is always selected"; vLLM API docs of
+// MiniMaxM3SparseAiterPAMetadataBuilder: the page-16 rebase B*16 + j).
+//
+// One CTA of 512 threads per row.  Scores become order-preserving uint32
+// keys (-0 folded onto +0) kept in shared memory.  A most-significant-digit
+// radix select (four 8-bit passes, shared-memory histograms, one warp scans
+// the 256 bins) finds the k'-th largest key tau and how many keys equal to
+// tau still fit.  Selection is then "key > tau, or key == tau and among the
+// first `need` such keys in page order" -- the lower page wins a tie --
+// computed with a block-wide prefix count in page order, and a second prefix
+// count over the selection flags gives each selected page its output slot,
+// so the table comes out in ascending page order without a sort.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bsp {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSmemKeys = 16384;  // rows with more candidates read keys from global memory
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// exclusive prefix sum over the block; returns this thread's offset and the total
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kThreads / 32) s_warp[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  total = s_warp[kThreads / 32 - 1];
+  const int before = (warp ? s_warp[warp - 1] : 0) + x - v;
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
+  extern __shared__ uint32_t s_keys[];
+  __shared__ int s_hist[256];
+  __shared__ int s_warp[kThreads / 32];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_gt;
+
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int max_len = p.max_pages * kPage;
+  const int L = min(max(p.row_len[r], 0), max_len);
+  const int n = (L + kPage - 1) / kPage;
+  const int kk = min(p.k_pages, n);
+  int32_t* ti = p.topk_idx + static_cast<int64_t>(r) * p.k_pages;
+  int32_t* bt = p.sparse_bt + static_cast<int64_t>(r) * p.k_pages;
+  for (int m = kk + tid; m < p.k_pages; m += kThreads) ti[m] = bt[m] = -1;
+  if (kk == 0) {
+    if (tid == 0) p.sparse_ctx[r] = 0;
+    return;
+  }
+  const int n_cand = p.force_tail ? n - 1 : n;
+  const int need = p.force_tail ? kk - 1 : kk;
+  const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
+  const bool in_smem = n_cand <= kSmemKeys;
+  auto key_at = [&](int i) -> uint32_t { return in_smem ? s_keys[i] : order_key(srow[i]); };
+
+  // need >= n_cand: every candidate; need == 0: none; else a radix select
+  const bool all = need >= n_cand, none = need == 0;
+  const bool radix = !all && !none;
+  uint32_t tau = 0;
+  int take_eq = 0;
+  if (radix) {
+    if (in_smem)
+      for (int i = tid; i < n_cand; i += kThreads) s_keys[i] = order_key(srow[i]);
+    uint32_t prefix = 0, mask = 0;
+    int krem = need;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      if (tid < 256) s_hist[tid] = 0;
+      __syncthreads();
+      for (int i = tid; i < n_cand; i += kThreads) {
+        const uint32_t k = key_at(i);
+        if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        // lane owns bins 255-8*lane .. 248-8*lane (descending); find the digit
+        // where the running count from the top first reaches krem
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = s_hist[255 - 8 * tid - j];
+          sum += c[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += y;
+        }
+        int run = incl - sum;  // keys in higher bins
+        if (run < krem && krem <= incl) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run < krem && krem <= run + c[j]) {
+              s_digit = static_cast<uint32_t>(255 - 8 * tid - j);
+              s_gt = run;
+            }
+            run += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      krem -= s_gt;
+      prefix |= s_digit << shift;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    tau = prefix;
+    take_eq = krem;
+  } else if (in_smem) {
+    for (int i = tid; i < n_cand; i += kThreads) s_keys[i] = 0xFFFFFFFFu;  // unused
+  }
+
+  // each thread owns a contiguous run of candidates, in page order
+  const int per = (n_cand + kThreads - 1) / kThreads;
+  const int b = min(tid * per, n_cand), e = min(b + per, n_cand);
+  int n_eq = 0;
+  if (radix)
+    for (int i = b; i < e; ++i) n_eq += key_at(i) == tau;
+  int tot;
+  int eq_before = block_exclusive_scan(n_eq, s_warp, tot);
+  int n_sel = 0;
+  {
+    int eqr = eq_before;
+    for (int i = b; i < e; ++i) {
+      bool sel = !none;
+      if (radix) {
+        const uint32_t k = key_at(i);
+        sel = k > tau || (k == tau && eqr < take_eq);
+        eqr += k == tau;
+      }
+      n_sel += sel;
+    }
+  }
+  int sel_before = block_exclusive_scan(n_sel, s_warp, tot);
+  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  {
+    int eqr = eq_before, pos = sel_before;
+    for (int i = b; i < e; ++i) {
+      bool sel = !none;
+      if (radix) {
+        const uint32_t k = key_at(i);
+        sel = k > tau || (k == tau && eqr < take_eq);
+        eqr += k == tau;
+      }
+      if (sel && pos < need) {  // exactly `need` are selected; the bound keeps writes in the row
+        ti[pos] = i;
+        bt[pos] = p.block_table[bt_row + i / kPagesPerSide] * p.id_mul + i % kPagesPerSide;
+        ++pos;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int tail_len = L - kPage * (n - 1);
+    if (p.force_tail) {
+      const int i = n - 1;
+      ti[kk - 1] = i;
+      bt[kk - 1] = p.block_table[bt_row + i / kPagesPerSide] * p.id_mul + i % kPagesPerSide;
+      p.sparse_ctx[r] = kPage * (kk - 1) + tail_len;
+    } else {
+      // the tail page, if selected, is the last entry
+      p.sparse_ctx[r] = kPage * (kk - 1) + (ti[kk - 1] == n - 1 ? tail_len : kPage);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
+  if (p.num_rows == 0) return cudaSuccess;
+  const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
+  const size_t bytes = static_cast<size_t>(cand) * 4;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  topk_select_kernel<<<p.num_rows, kThreads, bytes, s>>>(p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace bsp

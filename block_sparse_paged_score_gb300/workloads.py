@@ -185,7 +185,8 @@ class Workload:
         for s in range(self.num_decode):
             L = int(self.decode_lens[s])
             for j in range(self.q_len):
-                out.append((s, L - self.q_len + j))
+                if L - self.q_len + j >= 0:
+                    out.append((s, L - self.q_len + j))
         for c, (end, n) in enumerate(self.prefill_chunks):
             for p in range(end - n, end):
                 out.append((self.num_decode + c, p))

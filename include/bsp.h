@@ -202,7 +202,8 @@ bsp_status bsp_row_lengths_prefill(const int32_t* query_req_id, const int32_t* q
  *             decode query length).  The key cache of a sequence is streamed
  *             once per group, not once per row.  Every row of a group must
  *             name the same sequence (else BSP_DEVERR_GROUP_SEQ).
- *   max_pages width of the score rows; L_r is clamped to max_pages*16.
+ *   max_pages width of the score rows; L_r is clamped to max_pages*16;
+ *             max_pages <= 8 * bt_stride (the table covers every page).
  *   scores    fp32 [rows, max_pages], every element written.
  * Dot products run on tensor cores (mma.sync, fp16/bf16 operands that hold
  * the dequantised values exactly, fp32 accumulation).
@@ -288,30 +289,33 @@ bsp_status bsp_sparse_pa_prefill(const bsp_kv_cache* kv, const void* q, int32_t 
                                  int32_t k_pages, float sm_scale, void* out, int32_t* dev_err, bsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * The whole decode step as one call: write the step's new tokens, compute
- * the row lengths, score, select and attend.  All pointers are device
- * pointers; buffers are caller-owned.  `events` (nullable) receives 6
- * cudaEventRecord calls on `stream`: before the write, before scoring, before
- * the selection, before the attention, before the merge, and at the end.
+ * The whole decode step as one call: write the step's new tokens, cast the
+ * queries the writer emits as e4m3, compute the row lengths, score, select
+ * and attend.  All pointers are device pointers; buffers are caller-owned.
+ * `events` (nullable) receives 5 cudaEventRecord calls on `stream`: before
+ * the write, before scoring, before the selection, before the attention, and
+ * at the end.
  * ---------------------------------------------------------------------- */
 typedef struct bsp_decode_step_args {
   const bsp_kv_cache* kv;
-  const bsp_index_cache* idx;
+  const bsp_index_cache* idx;   /* idx->num_heads == kv->num_kv_heads */
   /* new tokens: k, v bf16 [T, Hkv, 128], idx_k bf16 [T, Hidx, 128], slot [T] */
   const void* k_new;
   const void* v_new;
   const void* idx_k_new;
   const int64_t* slot;
   int32_t num_new_tokens;
-  /* queries of the step: num_seqs * q_len tokens */
-  const void* q;          /* [tokens, Hkv*G, 128] of q_dtype */
-  int32_t q_dtype;
+  /* queries of the step (num_seqs * q_len tokens), bf16 as the model emits them */
+  const void* q;              /* bf16 [tokens, Hkv*G, 128] */
+  int32_t q_dtype;            /* BSP_BF16: attend with q; BSP_FP8_E4M3: cast into q_cast first */
+  void* q_cast;               /* uint8 [tokens, Hkv*G, 128] when q_dtype is e4m3, else unused */
   int32_t num_q_heads;
-  const void* idx_q;      /* [tokens, Hidx, 128] of idx_q_dtype */
-  int32_t idx_q_dtype;
+  const void* idx_q;          /* bf16 [tokens, Hidx, 128] */
+  int32_t idx_q_dtype;        /* as q_dtype, with idx_q_cast */
+  void* idx_q_cast;
   const int32_t* seq_lens;    /* [num_seqs], including the new tokens */
   int32_t num_seqs;
-  int32_t q_len;
+  int32_t q_len;              /* 1..8 */
   const int32_t* block_table; /* [num_seqs, bt_stride] */
   int32_t bt_stride;
   int32_t max_pages;
@@ -326,7 +330,7 @@ typedef struct bsp_decode_step_args {
   int32_t* sparse_bt;         /* [rows, k_pages] */
   int32_t* sparse_ctx;        /* [rows] */
   void* out;                  /* bf16 [tokens, Hkv*G, 128] */
-  void* ws;
+  void* ws;                   /* bsp_sparse_pa_decode_workspace_bytes(rows, k_pages, G) */
   size_t ws_bytes;
   int32_t* dev_err;
 } bsp_decode_step_args;

@@ -1,0 +1,65 @@
+"""The C ABI library builds, loads and exports every call include/bsp.h
+declares; host-side argument validation answers without touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bsp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(bsp_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_paged_score_gb300 import build
+    path = build.build()
+    return C.CDLL(path)
+
+
+def test_header_declares_the_five_steps():
+    names = declared_functions()
+    for n in ("bsp_kv_page_write", "bsp_index_score", "bsp_topk_select", "bsp_sparse_pa_decode",
+              "bsp_sparse_pa_prefill", "bsp_index_score_prefill", "bsp_sparse_decode_step"):
+        assert n in names, n
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_the_header():
+    from block_sparse_paged_score_gb300 import bsp
+    assert set(declared_functions()) <= set(bsp.SYMBOLS), set(declared_functions()) - set(bsp.SYMBOLS)
+
+
+def test_host_validation_without_a_gpu():
+    from block_sparse_paged_score_gb300 import bsp
+    L = bsp.lib()
+    assert L.bsp_status_str(2) == b"unsupported size or dtype"
+    assert L.bsp_kv_block_bytes(bsp.FP8_E4M3, 1) == 32768
+    assert L.bsp_kv_block_bytes(bsp.MXFP4, 1) == 2 * 8704
+    assert L.bsp_index_field_bytes(bsp.FP8_E4M3) == 16896
+    d = bsp.KvCacheDesc()
+    fake = 1 << 20  # a host-side descriptor only; never dereferenced here
+    assert L.bsp_kv_cache_interleaved(bsp.FP8_E4M3, 1, fake, 128, 0.5, 0.5, C.byref(d)) == 0
+    assert d.num_ids == 2040 and d.v_base - d.k_base == 8 * 2048 and d.id_stride_bytes == 2048
+    assert L.bsp_kv_cache_interleaved(bsp.MXFP4, 2, fake, 4, 1, 1, C.byref(d)) == 0
+    assert d.id_stride_bytes == 4 * 8704 and d.v_base - d.k_base == 2 * 8704 and d.num_ids == 32
+    assert L.bsp_kv_cache_interleaved(bsp.FP8_E4M3, 1, fake + 8, 128, 0.5, 0.5, C.byref(d)) == 1  # misaligned
+    ic = bsp.IndexCacheDesc()
+    assert L.bsp_index_cache_packed(bsp.FP8_E4M3, 1, fake, 16, C.byref(ic)) == 0
+    # q_group out of range and an MXFP4 prefill scorer are refused before any launch
+    assert L.bsp_index_score(C.byref(ic), fake, bsp.FP8_E4M3, fake, 4, fake, fake, 4, 9, 8, fake, None, None) == 2
+    ic2 = bsp.IndexCacheDesc()
+    assert L.bsp_index_cache_packed(bsp.MXFP4, 1, fake, 16, C.byref(ic2)) == 0
+    assert L.bsp_index_score_prefill(C.byref(ic2), fake, bsp.FP8_E4M3, fake, 4, fake, fake, 4, fake, 1, 1, 8, fake,
+                                     None, None) == 2
+    assert L.bsp_topk_select(fake, 4, 8, fake, fake, fake, 1, 0, 0, 1, fake, fake, fake, None) == 1  # k_pages 0

@@ -1,0 +1,262 @@
+"""Parity of the CUDA path with the CPU oracle on small seeded workloads that
+span several tiles, pages and blocks with ragged tails (GPU required).
+
+Stage by stage, each GPU stage gets inputs that both sides computed
+identically or that the oracle computed (never the other way round):
+  write      byte-exact cache bytes;
+  scores     |gpu - oracle| <= 2e-5 * sum_d |q_d k_d| (fp32 accumulation of
+             128 exact products), -inf pattern identical;
+  top-k      bit-exact when the GPU selector is fed the oracle's scores;
+  attention  max-abs 1e-2 and relative-L2 5e-3 (bf16 out) when the GPU
+             attention is fed the oracle's sparse table.
+End to end, the GPU pipeline and the oracle pipeline run independently and
+their selections agree up to near-ties (gap-aware comparison).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_sparse_paged_score_gb300 import workloads as W
+
+from harness import MINI, SM_SCALE, GpuSide, OracleSide, attention_close, bf16_f32, mini, selection_agrees
+
+pytestmark = pytest.mark.gpu
+
+SCORE_REL = 2e-5
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    from block_sparse_paged_score_gb300 import bsp as b
+    b.lib()
+    return b
+
+
+_cache = {}
+
+
+def sides(name):
+    if name not in _cache:
+        w = mini(name)
+        _cache[name] = (w, OracleSide(w), GpuSide(w))
+    return _cache[name]
+
+
+def test_cast_e4m3_byte_exact(bsp):
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(5000) * s for s in (1e-4, 1, 100, 1000)] + [[0.0, -0.0, 448, 464, 1e9]])
+    xb = W.to_bf16_bits(x.astype(np.float32))
+    xb = np.concatenate([xb, np.zeros((-len(xb)) % 8 + 3, np.uint16)])  # ragged tail
+    got = bsp.cast_e4m3(torch.from_numpy(xb.view(np.int16)).cuda()).cpu().numpy()
+    assert np.array_equal(got, O.cast_e4m3(xb))
+
+
+@pytest.mark.parametrize("name", list(MINI))
+def test_write_byte_exact(bsp, name):
+    w, o, g = sides(name)
+    torch.cuda.synchronize()
+    assert g.err.item() == 0
+    kv = g.kv.buffer.cpu().numpy()
+    idx = g.idx.buffer.cpu().numpy()
+    bad = np.nonzero(kv != o.kv)[0]
+    assert bad.size == 0, f"{bad.size} K/V bytes differ, first at {bad[:8]}"
+    bad = np.nonzero(idx != o.idx)[0]
+    assert bad.size == 0, f"{bad.size} index bytes differ, first at {bad[:8]}"
+
+
+@pytest.mark.parametrize("name", list(MINI))
+def test_step_write_is_idempotent_and_queries_cast(bsp, name):
+    w, o, g = sides(name)
+    k, v, ik, slot = w.step_tokens()
+    before = g.kv.buffer.clone()
+    if len(slot):
+        bsp.kv_page_write(g.kv, g.idx, g.t(k), g.t(v), g.t(ik), g.t(slot))
+    assert torch.equal(before, g.kv.buffer)
+    assert np.array_equal(g.q.cpu().numpy().view(o.q.dtype).reshape(o.q.shape), o.q)
+    assert np.array_equal(g.idx_q.cpu().numpy().view(o.idx_q.dtype).reshape(o.idx_q.shape), o.idx_q)
+
+
+@pytest.mark.parametrize("name", list(MINI))
+def test_row_lengths(bsp, name):
+    w, o, g = sides(name)
+    rs, rl = g.row_lengths()
+    assert np.array_equal(rs.cpu().numpy(), o.row_seq)
+    assert np.array_equal(rl.cpu().numpy(), o.row_len)
+
+
+@pytest.mark.parametrize("name", list(MINI))
+def test_index_score_within_bound(bsp, name):
+    w, o, g = sides(name)
+    ref, mag = o.scores(want_absdot=True)
+    rs, rl = g.row_lengths()
+    # decode rows share sequences in groups of q_len; the prefill part runs with q_group 1
+    nd = w.num_decode_rows
+    sc = torch.empty((w.num_rows, w.max_pages), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hidx = w.hidx
+    if nd:
+        bsp.index_score(g.idx, g.idx_q[:w.num_decode_tokens], w.idx_q_dtype, g.block_table, rs[:nd], rl[:nd],
+                        w.q_len, w.max_pages, scores=sc[:nd], dev_err=err)
+    if w.num_rows > nd:
+        bsp.index_score(g.idx, g.idx_q[w.num_decode_tokens:], w.idx_q_dtype, g.block_table, rs[nd:], rl[nd:],
+                        1, w.max_pages, scores=sc[nd:], dev_err=err)
+    got = sc.cpu().numpy()
+    assert err.item() == 0
+    inf_ref, inf_got = np.isneginf(ref), np.isneginf(got)
+    assert np.array_equal(inf_ref, inf_got)
+    fin = ~inf_ref
+    diff = np.abs(got[fin] - ref[fin])
+    bound = SCORE_REL * mag[fin] + 1e-30
+    ratio = float((diff / np.maximum(mag[fin], 1e-30)).max()) if diff.size else 0.0
+    assert (diff <= bound).all(), f"max |err|/sum|qk| = {ratio:.3g}"
+    print(f"{name}: max |err|/sum|qk| = {ratio:.3g} over {diff.size} pages")
+    _cache[name + ":scores"] = (ref, mag)
+
+
+@pytest.mark.parametrize("name", list(MINI))
+def test_topk_bit_exact_on_oracle_scores(bsp, name):
+    w, o, g = sides(name)
+    ref = o.scores()
+    ti, sb, ctx = o.topk(ref)
+    rs, rl = g.row_lengths()
+    gti, gsb, gctx = bsp.topk_select(torch.from_numpy(ref).cuda(), rs, rl, g.block_table, w.kv_dtype, w.k_pages)
+    assert np.array_equal(gti.cpu().numpy(), ti)
+    assert np.array_equal(gsb.cpu().numpy(), sb)
+    assert np.array_equal(gctx.cpu().numpy(), ctx)
+
+
+@pytest.mark.parametrize("force_tail", [True, False])
+@pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
+def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype):
+    rng = np.random.default_rng(3)
+    rows, max_pages = 300, 700
+    sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
+    sc[::5] = rng.standard_normal((len(sc[::5]), max_pages)).astype(np.float32)
+    sc[7, ::3] = -0.0
+    sc[8] = 0.0
+    L = rng.integers(0, max_pages * 16 + 1, rows).astype(np.int32)
+    L[:6] = [0, 1, 16, 17, max_pages * 16, max_pages * 16 - 1]
+    nblk = (max_pages + 7) // 8
+    bt = np.stack([rng.permutation(4 * nblk)[:nblk] for _ in range(rows)]).astype(np.int32)
+    rs = np.arange(rows, dtype=np.int32)
+    for k in (1, 2, 37, 128):
+        ti, sb, ctx = O.topk_select(sc, rs, L, bt, 1 if kv_dtype == W.MXFP4 else 0, k, force_tail)
+        gti, gsb, gctx = bsp.topk_select(torch.from_numpy(sc).cuda(), torch.from_numpy(rs).cuda(),
+                                         torch.from_numpy(L).cuda(), torch.from_numpy(bt).cuda(), kv_dtype, k,
+                                         flags=bsp.FORCE_TAIL if force_tail else 0)
+        assert np.array_equal(gti.cpu().numpy(), ti), k
+        assert np.array_equal(gsb.cpu().numpy(), sb), k
+        assert np.array_equal(gctx.cpu().numpy(), ctx), k
+
+
+@pytest.mark.parametrize("prefill", [False, True])
+@pytest.mark.parametrize("name", list(MINI))
+def test_attention_on_oracle_table(bsp, name, prefill):
+    w, o, g = sides(name)
+    ti, sb, ctx = o.topk(o.scores())
+    ref = bf16_f32(torch.from_numpy(o.attention(sb, ctx).view(np.int16)))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fn = bsp.sparse_pa_prefill if prefill else bsp.sparse_pa_decode
+    out = fn(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb).cuda(), torch.from_numpy(ctx).cuda(), w.k_pages,
+             SM_SCALE, dev_err=err)
+    got = bf16_f32(out).reshape(ref.shape)
+    assert err.item() == 0
+    ok, mx, rl2 = attention_close(got, ref)
+    print(f"{name} prefill={prefill}: worst err/allowed {mx:.3g} rel-L2 {rl2:.3g}")
+    assert ok, (mx, rl2)
+    # rows with nothing to attend are exactly zero
+    z = np.repeat(ctx == 0, w.group)
+    assert (got[z] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx"])
+def test_pipeline_end_to_end(bsp, name):
+    """GPU path and oracle path run independently from the same inputs."""
+    w, o, g = sides(name)
+    ref_sc, mag = o.scores(want_absdot=True)
+    ti, sb, ctx = o.topk(ref_sc)
+    rs, rl = g.row_lengths()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc = bsp.index_score(g.idx, g.idx_q, w.idx_q_dtype, g.block_table, rs, rl, w.q_len, w.max_pages, dev_err=err)
+    gti, gsb, gctx = bsp.topk_select(sc, rs, rl, g.block_table, w.kv_dtype, w.k_pages)
+    out = bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, gsb, gctx, w.k_pages, SM_SCALE, dev_err=err)
+    gti, gctx = gti.cpu().numpy(), gctx.cpu().numpy()
+    same = []
+    for r in range(w.num_rows):
+        ok, swaps = selection_agrees(gti[r], ti[r], ref_sc[r], o.row_len[r], w.k_pages,
+                                     SCORE_REL * float(mag[r].max()))
+        assert ok, f"row {r}: gpu {gti[r]} oracle {ti[r]}"
+        same.append(swaps == 0)
+    same = np.array(same)
+    assert np.array_equal(gctx[same], ctx[same])
+    ref = bf16_f32(torch.from_numpy(o.attention(sb, ctx).view(np.int16))).reshape(w.num_rows, w.group, 128)
+    got = bf16_f32(out).reshape(w.num_rows, w.group, 128)
+    ok, mx, rl2 = attention_close(got[same], ref[same])
+    assert ok, (mx, rl2)
+    assert err.item() == 0
+    print(f"{name}: {int((~same).sum())} rows with near-tie swaps; worst err/allowed {mx:.3g} rel-L2 {rl2:.3g}")
+
+
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx", "bf16"])
+def test_decode_step_matches_ops(bsp, name):
+    """bsp_sparse_decode_step == the separate calls, bit for bit."""
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides(name)
+    st = step.DecodeStep(w, g.kv, g.idx, g.block_table)
+    k, v, ik, slot = w.step_tokens()
+    st.run(g.t(k), g.t(v), g.t(ik), g.t(slot), g.q_bf16, g.idx_q_bf16, g.t(w.decode_lens))
+    rs, rl = g.row_lengths()
+    sc = bsp.index_score(g.idx, g.idx_q, w.idx_q_dtype, g.block_table, rs, rl, w.q_len, w.max_pages)
+    gti, gsb, gctx = bsp.topk_select(sc, rs, rl, g.block_table, w.kv_dtype, w.k_pages)
+    out = bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, gsb, gctx, w.k_pages, SM_SCALE)
+    assert torch.equal(st.scores, sc)
+    assert torch.equal(st.sparse_bt, gsb) and torch.equal(st.sparse_ctx, gctx)
+    assert torch.equal(st.out, out)
+    assert st.dev_err.item() == 0
+
+
+def test_device_errors_are_flagged_not_faulted(bsp):
+    w, o, g = sides("fp8")
+    rows = 4
+    sb = torch.full((rows, w.k_pages), 0, dtype=torch.int32, device="cuda")
+    sb[1, 0] = int(g.kv.desc.num_ids)  # out of range
+    sb[2, 0] = -5
+    ctx = torch.full((rows,), 16, dtype=torch.int32, device="cuda")
+    q = g.q[:rows]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bsp.sparse_pa_decode(g.kv, q, w.q_dtype, w.hq, sb, ctx, w.k_pages, SM_SCALE, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & 1  # BSP_DEVERR_PAGE_ID
+    # a block table entry beyond the index cache
+    bt = g.block_table.clone()
+    bt[0, 0] = w.num_blocks + 3
+    err.zero_()
+    rs, rl = g.row_lengths()
+    bsp.index_score(g.idx, g.idx_q, w.idx_q_dtype, bt, rs, rl, 1, w.max_pages, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & 2
+    # a slot beyond the cache
+    err.zero_()
+    k = torch.zeros((1, w.hkv, 128), dtype=torch.int16, device="cuda")
+    slot = torch.tensor([w.num_blocks * 128 + 5], dtype=torch.int64, device="cuda")
+    bsp.kv_page_write(g.kv, g.idx, k, k, k[:, :w.hidx], slot, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() & 16
+
+
+def test_host_argument_errors(bsp):
+    w, o, g = sides("fp8")
+    rs, rl = g.row_lengths()
+    with pytest.raises(bsp.BspError) as e:
+        bsp.index_score(g.idx, g.idx_q, w.idx_q_dtype, g.block_table, rs, rl, 9, w.max_pages)  # q_group > 8
+    assert e.value.status == 2
+    ti, sb, ctx = o.topk(o.scores())
+    with pytest.raises(bsp.BspError) as e:  # 12 query heads per KV head
+        bsp.sparse_pa_decode(g.kv, g.q[:, :12].contiguous(), w.q_dtype, 12, torch.from_numpy(sb).cuda(),
+                             torch.from_numpy(ctx).cuda(), w.k_pages)
+    assert e.value.status == 2
+    with pytest.raises(bsp.BspError) as e:  # workspace too small
+        bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb).cuda(), torch.from_numpy(ctx).cuda(),
+                             w.k_pages, ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 3
