@@ -58,6 +58,26 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def rank_workload_spec(config, rank):
+    """Each rank runs its own batch: the configuration's shapes with seeds
+    offset by the rank (weak scaling; nothing is exchanged between ranks)."""
+    from block_sparse_paged_score_gb300 import workloads as W
+    spec = dict(W.CONFIGS[config])
+    spec["seed"] = spec["seed"] + 1000 * rank
+    return spec
+
+
+def max_over_ranks(x, device=None):
+    """The slowest rank's figure (a no-op without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -264,9 +284,7 @@ def run_ours(args):
     from block_sparse_paged_score_gb300 import bsp, step, workloads as W
 
     bsp.lib()
-    spec = dict(W.CONFIGS[args.config])
-    spec["seed"] = spec["seed"] + 1000 * rank  # each rank its own batch
-    w = W.Workload(spec)
+    w = W.Workload(rank_workload_spec(args.config, rank))
 
     def t(a):
         a = np.ascontiguousarray(a)
@@ -323,11 +341,7 @@ def run_ours(args):
     step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(K)]
     score_ms = [events[i][1].elapsed_time(events[i][2]) for i in range(K)]
     attn_ms = [events[i][3].elapsed_time(events[i][4]) for i in range(K)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(statistics.mean(step_ms), dev)
     tokens = w.num_decode_tokens + (w.num_prefill_tokens if mixed else 0)
     value = tokens * world / (ms / 1e3)
 
@@ -363,11 +377,7 @@ def run_ours(args):
             hs.run(stream)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        e_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), dev)
         e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": hs.h2d_bytes, "d2h_bytes_per_step": hs.d2h_bytes}
 
