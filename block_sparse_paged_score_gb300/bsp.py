@@ -70,6 +70,9 @@ SYMBOLS = {
     "bsp_sparse_pa_decode": [C.POINTER(KvCacheDesc), C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                              C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p,
                              C.c_void_p],
+    "bsp_sparse_pa_decode_noalloc": [C.POINTER(KvCacheDesc), C.c_void_p, C.c_int32, C.c_int32, C.c_void_p,
+                                     C.c_void_p, C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_void_p,
+                                     C.c_void_p],
     "bsp_sparse_pa_prefill": [C.POINTER(KvCacheDesc), C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                               C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p],
     "bsp_sparse_pa_decode_workspace_bytes": [C.c_int32, C.c_int32, C.c_int32],
@@ -260,6 +263,20 @@ def sparse_pa_decode(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, k_pages
            lib().bsp_sparse_pa_decode(C.byref(kv.desc), _ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
                                       _ptr(sparse_ctx), rows, k_pages, sm_scale, _ptr(out), _ptr(ws), ws.numel(),
                                       _ptr(dev_err), _stream(stream)))
+    return out
+
+
+def sparse_pa_decode_noalloc(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, k_pages, sm_scale=None, out=None,
+                             dev_err=None, stream=None):
+    """bsp_sparse_pa_decode without a caller workspace (the library's own
+    fixed scratch; see include/bsp.h for the size limit and the sharing rule)."""
+    rows = sparse_ctx.numel()
+    sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(128)
+    out = out if out is not None else torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _check("bsp_sparse_pa_decode_noalloc",
+           lib().bsp_sparse_pa_decode_noalloc(C.byref(kv.desc), _ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
+                                              _ptr(sparse_ctx), rows, k_pages, sm_scale, _ptr(out), _ptr(dev_err),
+                                              _stream(stream)))
     return out
 
 

@@ -277,6 +277,32 @@ bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q
                                 int32_t* dev_err, bsp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * bsp_sparse_pa_decode_noalloc -- the same computation as bsp_sparse_pa_decode
+ * for callers that cannot allocate device memory, and so cannot provide the
+ * split-K workspace: code embedded in a host application that plans and
+ * reserves all device memory up front and forbids allocation afterwards, or
+ * a caller reaching this ABI from a runtime with no device allocator at hand.
+ * The pages have no counterpart to this call; it exists only for such
+ * callers.
+ *  - The workspace is a scratch array inside the library, a file-scope
+ *    __device__ array of 16 MiB that every GPU loading the library holds
+ *    until the process exits.  A call whose split-K plan needs more
+ *    (bsp_sparse_pa_decode_workspace_bytes(rows, k_pages, G) > 16 MiB) returns
+ *    BSP_ERR_WORKSPACE and enqueues nothing.
+ *  - The first call on a device looks up the array's address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Calls share the array: calls that overlap on the GPU (other streams,
+ *    other host threads) race on it and must be serialised by the caller.
+ *  - It calls no allocator (no cudaMalloc / cudaFree).  Arguments and errors
+ *    are those of bsp_sparse_pa_decode.
+ * ---------------------------------------------------------------------- */
+bsp_status bsp_sparse_pa_decode_noalloc(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
+                                        const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
+                                        int32_t k_pages, float sm_scale, void* out, int32_t* dev_err,
+                                        bsp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * a5  bsp_sparse_pa_prefill -- the same attention for prefill rows, one row
  * per (prefill token, KV head), each with its own sparse table and a context
  * length from its absolute position ([MSA-API] forward: the prefill call with
