@@ -248,8 +248,9 @@ def decode_workspace_bytes(num_rows, k_pages, group):
 
 
 def decode_workspace(num_rows, k_pages, group, device="cuda"):
+    """A zeroed split-K workspace (its arrival counters must start at zero)."""
     n = decode_workspace_bytes(num_rows, k_pages, group)
-    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
 def sparse_pa_decode(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, k_pages, sm_scale=None, out=None, ws=None,

@@ -290,8 +290,8 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group) {
   (void)group;
   if (num_rows <= 0 || k_pages <= 0) return 0;
-  int32_t ns, pps;
-  sparse_pa_plan(num_rows, k_pages, device_sms(), &ns, &pps);
+  int32_t ns, pps, cl;
+  sparse_pa_plan(num_rows, k_pages, device_sms(), &ns, &pps, &cl);
   return sparse_pa_ws_bytes(num_rows, ns);
 }
 
@@ -328,7 +328,7 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   p.out = out;
   p.err = dev_err;
   if (decode) {
-    sparse_pa_plan(num_rows, k_pages, device_sms(), &p.nsplit, &p.pages_per_split);
+    sparse_pa_plan(num_rows, k_pages, device_sms(), &p.nsplit, &p.pages_per_split, &p.cluster);
     const size_t need = sparse_pa_ws_bytes(num_rows, p.nsplit);
     if (need) {
       if (!ws || ws_bytes < need || !al(ws, 16)) return BSP_ERR_WORKSPACE;
@@ -371,24 +371,61 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
     if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s);
   };
   mark(0);
-  bsp_status st = bsp_kv_page_write(a->kv, a->idx, a->k_new, a->v_new, a->idx_k_new, a->slot, a->num_new_tokens,
-                                    a->dev_err, stream);
+  // write + e4m3 casts + row lengths: one launch
+  bsp_status st = check_kv(a->kv);
   if (st != BSP_OK) return st;
+  if ((st = check_idx(a->idx)) != BSP_OK) return st;
+  if (a->num_new_tokens < 0 || a->num_q_heads < 1) return BSP_ERR_INVALID_ARG;
+  if (a->num_new_tokens && (!a->k_new || !a->v_new || !a->idx_k_new || !a->slot || !al(a->k_new, 16) ||
+                            !al(a->v_new, 16) || !al(a->idx_k_new, 16) || !al(a->slot, 8)))
+    return BSP_ERR_INVALID_ARG;
+  if (!a->q || !a->idx_q || !al(a->q, 16) || !al(a->idx_q, 16) || !a->seq_lens || !a->row_seq || !a->row_len)
+    return BSP_ERR_INVALID_ARG;
   const void* q = a->q;
   const void* iq = a->idx_q;
+  DecodePrepParams pp{};
+  KvWriteParams& w = pp.write;
+  w.kv_dtype = a->kv->dtype;
+  w.hkv = hkv;
+  w.k_base = static_cast<uint8_t*>(a->kv->k_base);
+  w.v_base = static_cast<uint8_t*>(a->kv->v_base);
+  w.id_stride = a->kv->id_stride_bytes;
+  w.num_blocks = a->kv->num_blocks;
+  w.k_scale = a->kv->k_scale;
+  w.v_scale = a->kv->v_scale;
+  w.idx_dtype = a->idx->dtype;
+  w.hidx = hidx;
+  w.idx_base = static_cast<uint8_t*>(a->idx->base);
+  w.idx_block_stride = a->idx->block_stride_bytes;
+  w.idx_num_blocks = a->idx->num_blocks;
+  w.k = static_cast<const uint16_t*>(a->k_new);
+  w.v = static_cast<const uint16_t*>(a->v_new);
+  w.idx_k = static_cast<const uint16_t*>(a->idx_k_new);
+  w.slot = a->slot;
+  w.num_tokens = a->num_new_tokens;
+  w.err = a->dev_err;
   if (a->q_dtype == BSP_FP8_E4M3) {
-    if ((st = bsp_cast_e4m3(a->q, a->q_cast, static_cast<int64_t>(tokens) * a->num_q_heads * kDim, stream)) != BSP_OK)
-      return st;
+    if (!a->q_cast || !al(a->q_cast, 8)) return BSP_ERR_INVALID_ARG;
+    pp.cast_src[0] = static_cast<const uint16_t*>(a->q);
+    pp.cast_dst[0] = static_cast<uint8_t*>(a->q_cast);
+    pp.cast_n[0] = static_cast<int64_t>(tokens) * a->num_q_heads * kDim;
     q = a->q_cast;
   }
   if (a->idx_q_dtype == BSP_FP8_E4M3) {
-    if ((st = bsp_cast_e4m3(a->idx_q, a->idx_q_cast, static_cast<int64_t>(tokens) * hidx * kDim, stream)) != BSP_OK)
-      return st;
+    if (!a->idx_q_cast || !al(a->idx_q_cast, 8)) return BSP_ERR_INVALID_ARG;
+    pp.cast_src[1] = static_cast<const uint16_t*>(a->idx_q);
+    pp.cast_dst[1] = static_cast<uint8_t*>(a->idx_q_cast);
+    pp.cast_n[1] = static_cast<int64_t>(tokens) * hidx * kDim;
     iq = a->idx_q_cast;
   }
-  if ((st = bsp_row_lengths_decode(a->seq_lens, a->num_seqs, a->q_len, hkv, a->row_seq, a->row_len, stream)) !=
-      BSP_OK)
-    return st;
+  pp.seq_lens = a->seq_lens;
+  pp.num_seqs = a->num_seqs;
+  pp.q_len = a->q_len;
+  pp.heads = hkv;
+  pp.row_seq = a->row_seq;
+  pp.row_len = a->row_len;
+  if ((st = cuda_status(launch_decode_prep(pp, s))) != BSP_OK) return st;
+  ++g_launches;
   mark(1);
   if ((st = bsp_index_score(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
                             a->q_len, a->max_pages, a->scores, a->dev_err, stream)) != BSP_OK)

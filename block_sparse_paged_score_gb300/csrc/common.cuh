@@ -119,6 +119,12 @@ __device__ __forceinline__ void e4m3x4_to_f16x2_scaled(uint32_t w, uint32_t& lo,
   lo = (a & 0x80008000u) | ((a >> 1) & 0x3F803F80u);
   hi = (b & 0x80008000u) | ((b >> 1) & 0x3F803F80u);
 }
+// Four e4m3 bytes -> two f16x2 with the hardware conversion (exact, no scale).
+__device__ __forceinline__ void e4m3x4_to_f16x2_cvt(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
 // Two e2m1 codes in one byte (first element in the low nibble) -> f16x2.
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;
@@ -177,6 +183,24 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
   __half2 h;
   *reinterpret_cast<uint32_t*>(&h) = w;
   return __half22float2(h);
+}
+
+// ---- thread-block clusters ------------------------------------------------
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// load a float at the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

@@ -16,11 +16,15 @@
 //   A = 16 keys x 16 dims (fp8 -> f16 exactly, e2m1 -> f16 exactly, or bf16),
 //   B = 16 dims x 8 query rows (the group's rows; unused columns are zero),
 //   C = fp32.
-// The dims of each mma are a permutation of 16 real dims chosen so that every
-// thread reads 16-byte (or 4-byte) runs of a key row; A and B use the same
-// permutation, so each dot product is unchanged.  The per-token fp8 scale and
+// fp8 keys with an e4m3 query run on the fp8 mma (m16n8k32 e4m3 x e4m3 ->
+// f32) straight from the cached bytes.  The dims of each mma are a
+// permutation of the real dims chosen so that every thread reads 16-byte (or
+// 4-byte) runs of a key row; A and B use the same permutation, so each dot
+// product is unchanged.  The per-token fp8 scale and
 // the per-32-dim e8m0 scales are applied to the fp32 partial sums, then the
 // page max is a shuffle reduction over the 16 tokens of the tile.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -45,10 +49,18 @@ struct KeyFmt<BSP_MXFP4> {
   static constexpr int kField = kMxField;
   static constexpr int kStages = 6;
 };
+// fp8 keys scored against an e4m3 query: the fp8 mma takes the cached bytes
+// as they are (no conversion)
+constexpr int kFp8KeysE4m3Q = 3;
+template <>
+struct KeyFmt<kFp8KeysE4m3Q> {
+  static constexpr int kField = kFp8IndexField;
+  static constexpr int kStages = 4;
+};
 
 template <int KEY>
-constexpr int smem_bytes() {
-  return KeyFmt<KEY>::kStages * KeyFmt<KEY>::kField + KeyFmt<KEY>::kStages * 8;
+constexpr int smem_bytes(int stages) {
+  return stages * KeyFmt<KEY>::kField + stages * 8;
 }
 
 // first of the four real dims that B fragment m of thread t covers
@@ -57,6 +69,16 @@ __device__ __forceinline__ int frag_dim(int m, int t) {
   if (KEY == BSP_FP8_E4M3) return 16 * (t + 4 * (m >> 2)) + 4 * (m & 3);
   if (KEY == BSP_MXFP4) return 32 * (m >> 1) + 8 * t + 4 * (m & 1);
   return 8 * (t + 4 * (m >> 1)) + 4 * (m & 1);
+}
+
+// D (16x8 f32) += A (16x32 e4m3, row) * B (32x8 e4m3, col)
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off, float (&v)[4]) {
@@ -76,10 +98,11 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off,
 template <int KEY>
 __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   constexpr int FB = KeyFmt<KEY>::kField;
-  constexpr int S = KeyFmt<KEY>::kStages;
+  const int S = p.stages;  // ring depth, 1..kStages
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * FB);
   __shared__ int s_len[8], s_row[8], s_seq;
+  __shared__ int s_bid[32];  // the chunk's block ids (blocks_per_chunk <= 32)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int group = blockIdx.x / p.hidx, h = blockIdx.x % p.hidx;
@@ -121,13 +144,18 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
       p.scores[static_cast<int64_t>(s_row[i / npg]) * p.max_pages + pfirst + i % npg] = -INFINITY;
   }
   if (nb == 0) return;
-
-  auto issue = [&](int i) {
-    int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + i];
+  if (tid < nb) {
+    int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + tid];
     if (bid < 0 || bid >= p.num_blocks) {
       set_err(p.err, BSP_DEVERR_BLOCK_ID);
       bid = 0;
     }
+    s_bid[tid] = bid;
+  }
+  __syncthreads();
+
+  auto issue = [&](int i) {
+    const int bid = s_bid[i];
     const int st = i % S;
     mbar_arrive_expect_tx(&bars[st], FB);
     bulk_g2s(smem + st * FB, p.idx_base + static_cast<int64_t>(bid) * p.block_stride + static_cast<int64_t>(h) * FB,
@@ -138,8 +166,19 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
 
   // B fragments: query row g of the group (zero beyond the group)
   uint32_t qb[8][2];
+  if (KEY == kFp8KeysE4m3Q) {
+    // mma m (< 4): this thread's 16-dim chunk c = t + 4*(m/2), dims 8*(m%2) + 0..7
+    const uint8_t* qrow = static_cast<const uint8_t*>(p.q) + (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int d = 16 * (t + 4 * (m >> 1)) + 8 * (m & 1);
+      qb[m][0] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+      qb[m][1] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d + 4) : 0u;
+    }
+  }
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
+    if (KEY == kFp8KeysE4m3Q) break;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     if (g < ntok) load_q4(p.q, p.q_dtype, (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim + frag_dim<KEY>(m, t), v);
     if (KEY == BSP_BF16) {
@@ -161,7 +200,20 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
     for (int tile = 0; tile < 2; ++tile) {
       const int tokb = 32 * warp + 16 * tile;
       float v0, v1, v2, v3;
-      if (KEY == BSP_FP8_E4M3) {
+      if (KEY == kFp8KeysE4m3Q) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ra_row = sbase + (tokb + g) * 128, rb_row = ra_row + 8 * 128;
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii) {
+          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+          mma_e4m3(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
+          mma_e4m3(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
+        }
+        const float sg = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g) * 4);
+        const float sg8 = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g + 8) * 4);
+        v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
+      } else if (KEY == BSP_FP8_E4M3) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const uint32_t ra_row = sbase + (tokb + g) * 128, rb_row = ra_row + 8 * 128;
 #pragma unroll
@@ -251,15 +303,36 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
 
 template <int KEY>
 cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
-  constexpr int bytes = smem_bytes<KEY>();
   static bool configured = false;  // per process; the attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes<KEY>(KeyFmt<KEY>::kStages));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  index_score_kernel<KEY><<<grid, 128, bytes, s>>>(p);
+  index_score_kernel<KEY><<<grid, 128, smem_bytes<KEY>(p.stages), s>>>(p);
   return cudaPeekAtLastError();
+}
+
+template <int KEY>
+void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
+  // Small problems: one block per CTA, one stage, every CTA resident at once
+  // (the whole batch is in flight from the start).  Large ones: 2..32 blocks
+  // per CTA through a deep ring, about four waves of resident CTAs.
+  const int64_t work = static_cast<int64_t>(p.num_groups) * p.hidx * max_blocks;
+  const int64_t slots1 = static_cast<int64_t>(num_sms) *
+                         std::min<int64_t>(16, (227 * 1024) / smem_bytes<KEY>(1));
+  if (work <= slots1) {
+    p.blocks_per_chunk = 1;
+    p.stages = 1;
+    return;
+  }
+  const int S = KeyFmt<KEY>::kStages;
+  const int64_t slots = static_cast<int64_t>(num_sms) * std::max<int64_t>(1, (227 * 1024) / smem_bytes<KEY>(S));
+  int64_t cb = (work + 4 * slots - 1) / (4 * slots);
+  cb = cb < 2 ? 2 : (cb > 32 ? 32 : cb);
+  p.blocks_per_chunk = static_cast<int32_t>(cb);
+  p.stages = static_cast<int32_t>(std::min<int64_t>(S, cb));
 }
 
 }  // namespace
@@ -268,16 +341,23 @@ cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) 
   if (p.num_rows == 0 || p.max_pages == 0) return cudaSuccess;
   p.num_groups = (p.num_tokens + p.q_group - 1) / p.q_group;
   const int64_t max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
-  // about four CTAs per SM of streaming work, 2..32 blocks per CTA
-  int64_t cb = (static_cast<int64_t>(p.num_groups) * p.hidx * max_blocks + 4 * num_sms - 1) / (4 * num_sms);
-  cb = cb < 2 ? 2 : (cb > 32 ? 32 : cb);
-  p.blocks_per_chunk = static_cast<int32_t>(cb);
+  switch (p.idx_dtype) {
+    case BSP_BF16:
+      plan_key<BSP_BF16>(p, max_blocks, num_sms);
+      break;
+    case BSP_FP8_E4M3:
+      plan_key<BSP_FP8_E4M3>(p, max_blocks, num_sms);  // same field and ring as the e4m3-query form
+      break;
+    default:
+      plan_key<BSP_MXFP4>(p, max_blocks, num_sms);
+  }
+  const int64_t cb = p.blocks_per_chunk;
   const dim3 grid(static_cast<unsigned>(p.num_groups * p.hidx), static_cast<unsigned>((max_blocks + cb - 1) / cb));
   switch (p.idx_dtype) {
     case BSP_BF16:
       return launch_key<BSP_BF16>(p, grid, s);
     case BSP_FP8_E4M3:
-      return launch_key<BSP_FP8_E4M3>(p, grid, s);
+      return p.q_dtype == BSP_FP8_E4M3 ? launch_key<kFp8KeysE4m3Q>(p, grid, s) : launch_key<BSP_FP8_E4M3>(p, grid, s);
     default:
       return launch_key<BSP_MXFP4>(p, grid, s);
   }

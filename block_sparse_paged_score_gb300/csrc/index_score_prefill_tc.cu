@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = sm.bars + 1 + 2 * kStages;
   uint64_t* acc_empty = sm.bars + 3 + 2 * kStages;
   __shared__ int s_tok0, s_tok1, s_lmax, s_seq;
+  __shared__ int s_bid[kKeyBlocksPerCta];  // the key range's block ids (-1: missing)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kb0 = blockIdx.y * kKeyBlocksPerCta;
@@ -192,6 +193,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
+  if (tid < nb) {
+    int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + kb0 + tid];
+    if (bid < 0 || bid >= p.num_blocks) {
+      set_err(p.err, BSP_DEVERR_BLOCK_ID);
+      bid = -1;
+    }
+    s_bid[tid] = bid;
+  }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(sm.tmem_slot)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -203,12 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto block_row = [&](int blk) -> int {
     if (blk >= kb0 + nb) return oob_row;
-    const int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk];
-    if (bid < 0 || bid >= p.num_blocks) {
-      set_err(p.err, BSP_DEVERR_BLOCK_ID);
-      return oob_row;
-    }
-    return bid * rows_per_block;
+    const int bid = s_bid[blk - kb0];
+    return bid < 0 ? oob_row : bid * rows_per_block;
   };
 
   if (warp == 0) {
@@ -254,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int blk = kb0 + 2 * j + (i >> 7);
         float s = 0.f;
         if (blk < kb0 + nb) {
-          const int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk];
-          if (bid >= 0 && bid < p.num_blocks)
+          const int bid = s_bid[blk - kb0];
+          if (bid >= 0)
             s = *reinterpret_cast<const float*>(p.idx_base + static_cast<int64_t>(bid) * p.block_stride +
                                                 kFp8IndexScaleOff + (i & 127) * 4);
         }

@@ -25,6 +25,20 @@ struct KvWriteParams {
   int32_t* err;
 };
 cudaError_t launch_kv_page_write(const KvWriteParams& p, cudaStream_t s);
+
+// write + the two e4m3 query casts + decode row lengths in one launch
+struct DecodePrepParams {
+  KvWriteParams write;
+  const uint16_t* cast_src[2];  // NULL: no cast
+  uint8_t* cast_dst[2];
+  int64_t cast_n[2];
+  const int32_t* seq_lens;
+  int32_t num_seqs, q_len, heads;
+  int32_t* row_seq;
+  int32_t* row_len;
+  int64_t write_blocks, cast_blocks[2];  // filled by the launcher
+};
+cudaError_t launch_decode_prep(DecodePrepParams p, cudaStream_t s);
 cudaError_t launch_cast_e4m3(const uint16_t* x, uint8_t* out, int64_t n, cudaStream_t s);
 cudaError_t launch_row_lengths_decode(const int32_t* seq_lens, int32_t num_seqs, int32_t q_len, int32_t heads,
                                       int32_t* row_seq, int32_t* row_len, cudaStream_t s);
@@ -42,7 +56,7 @@ struct IndexScoreParams {
   const int32_t* row_seq;
   const int32_t* row_len;
   int32_t num_rows, num_tokens, q_group, max_pages;
-  int32_t blocks_per_chunk, num_groups;
+  int32_t blocks_per_chunk, num_groups, stages;
   float* scores;
   int32_t* err;
 };
@@ -75,13 +89,17 @@ struct SparsePaParams {
   int32_t num_rows, k_pages;
   float sm_scale;
   void* out;
-  float* ws;  // partials, nsplit > 1
+  float* ws;  // partials when nsplit > 8 (not clustered)
   int32_t nsplit, pages_per_split;
+  int32_t cluster;  // 2..8: the row's splits form a cluster and merge on chip
   int32_t* err;
 };
 // split plan shared by the launcher and the workspace query
-void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split);
+void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split,
+                    int32_t* cluster);
 size_t sparse_pa_ws_bytes(int32_t num_rows, int32_t nsplit);
+// bytes of the per-row arrival counters at the start of the workspace
+size_t sparse_pa_counter_bytes(int32_t num_rows);
 cudaError_t launch_sparse_pa(const SparsePaParams& p, cudaStream_t s, int* launches);
 
 struct PrefillScoreParams {

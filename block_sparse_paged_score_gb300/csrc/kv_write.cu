@@ -41,9 +41,9 @@ __device__ __forceinline__ void write_mx(uint8_t* field, int o, int lane, const 
   if ((lane & 7) == 0) field[kMxScaleOff + o * 4 + (lane >> 3)] = static_cast<uint8_t>(e + 127);
 }
 
-__global__ void __launch_bounds__(128) kv_page_write_kernel(KvWriteParams p) {
+__device__ __forceinline__ void kv_page_write_block(const KvWriteParams& p, int64_t block_idx) {
   const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int64_t gw = block_idx * 4 + (threadIdx.x >> 5);
   const int units = 2 * p.hkv + p.hidx;
   const int64_t token = gw / units;
   const int u = static_cast<int>(gw % units);
@@ -126,8 +126,12 @@ __global__ void __launch_bounds__(128) kv_page_write_kernel(KvWriteParams p) {
   }
 }
 
-__global__ void cast_e4m3_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ out, int64_t n) {
-  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+__global__ void __launch_bounds__(128) kv_page_write_kernel(KvWriteParams p) { kv_page_write_block(p, blockIdx.x); }
+
+// 8 elements per thread, 128 threads per block
+__device__ __forceinline__ void cast_e4m3_block(const uint16_t* __restrict__ x, uint8_t* __restrict__ out, int64_t n,
+                                                int64_t block_idx) {
+  const int64_t i = (block_idx * 128 + threadIdx.x) * 8;
   if (i + 8 <= n) {
     const uint4 v = *reinterpret_cast<const uint4*>(x + i);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -144,9 +148,16 @@ __global__ void cast_e4m3_kernel(const uint16_t* __restrict__ x, uint8_t* __rest
   }
 }
 
-__global__ void row_lengths_decode_kernel(const int32_t* seq_lens, int32_t num_seqs, int32_t q_len, int32_t heads,
-                                          int32_t* row_seq, int32_t* row_len) {
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(128) cast_e4m3_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ out,
+                                                        int64_t n) {
+  cast_e4m3_block(x, out, n, blockIdx.x);
+}
+
+// 128 rows per block
+__device__ __forceinline__ void row_lengths_decode_block(const int32_t* seq_lens, int32_t num_seqs, int32_t q_len,
+                                                         int32_t heads, int32_t* row_seq, int32_t* row_len,
+                                                         int64_t block_idx) {
+  const int64_t r = block_idx * 128 + threadIdx.x;
   const int64_t rows = static_cast<int64_t>(num_seqs) * q_len * heads;
   if (r >= rows) return;
   const int64_t token = r / heads;
@@ -154,6 +165,26 @@ __global__ void row_lengths_decode_kernel(const int32_t* seq_lens, int32_t num_s
   const int64_t L = static_cast<int64_t>(seq_lens[s]) - (q_len - 1 - j);
   row_seq[r] = s;
   row_len[r] = static_cast<int32_t>(L < 0 ? 0 : L);
+}
+
+__global__ void __launch_bounds__(128) row_lengths_decode_kernel(const int32_t* seq_lens, int32_t num_seqs,
+                                                                 int32_t q_len, int32_t heads, int32_t* row_seq,
+                                                                 int32_t* row_len) {
+  row_lengths_decode_block(seq_lens, num_seqs, q_len, heads, row_seq, row_len, blockIdx.x);
+}
+
+// The decode step's preparation in one launch: blocks [0, w) write the new
+// tokens, the next blocks cast the two query tensors to e4m3, the last ones
+// compute the row lengths.  The parts are independent.
+__global__ void __launch_bounds__(128) decode_prep_kernel(DecodePrepParams p) {
+  int64_t b = blockIdx.x;
+  if (b < p.write_blocks) return kv_page_write_block(p.write, b);
+  b -= p.write_blocks;
+  for (int c = 0; c < 2; ++c) {
+    if (b < p.cast_blocks[c]) return cast_e4m3_block(p.cast_src[c], p.cast_dst[c], p.cast_n[c], b);
+    b -= p.cast_blocks[c];
+  }
+  row_lengths_decode_block(p.seq_lens, p.num_seqs, p.q_len, p.heads, p.row_seq, p.row_len, b);
 }
 
 __global__ void row_lengths_prefill_kernel(const int32_t* req, const int32_t* pos, int32_t n, int32_t heads,
@@ -177,8 +208,7 @@ cudaError_t launch_kv_page_write(const KvWriteParams& p, cudaStream_t s) {
 
 cudaError_t launch_cast_e4m3(const uint16_t* x, uint8_t* out, int64_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  const int64_t threads = (n + 7) / 8;
-  cast_e4m3_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(x, out, n);
+  cast_e4m3_kernel<<<static_cast<unsigned>((n + 1023) / 1024), 128, 0, s>>>(x, out, n);
   return cudaPeekAtLastError();
 }
 
@@ -186,8 +216,18 @@ cudaError_t launch_row_lengths_decode(const int32_t* seq_lens, int32_t num_seqs,
                                       int32_t* row_seq, int32_t* row_len, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(num_seqs) * q_len * heads;
   if (rows == 0) return cudaSuccess;
-  row_lengths_decode_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, s>>>(seq_lens, num_seqs, q_len,
+  row_lengths_decode_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, s>>>(seq_lens, num_seqs, q_len,
                                                                                        heads, row_seq, row_len);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_decode_prep(DecodePrepParams p, cudaStream_t s) {
+  p.write_blocks = (static_cast<int64_t>(p.write.num_tokens) * (2 * p.write.hkv + p.write.hidx) + 3) / 4;
+  for (int c = 0; c < 2; ++c) p.cast_blocks[c] = p.cast_src[c] ? (p.cast_n[c] + 1023) / 1024 : 0;
+  const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.q_len * p.heads;
+  const int64_t total = p.write_blocks + p.cast_blocks[0] + p.cast_blocks[1] + (rows + 127) / 128;
+  if (total == 0) return cudaSuccess;
+  decode_prep_kernel<<<static_cast<unsigned>(total), 128, 0, s>>>(p);
   return cudaPeekAtLastError();
 }
 

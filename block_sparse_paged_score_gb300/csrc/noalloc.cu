@@ -13,9 +13,11 @@
 // that loads the library holds it until the process exits.  The first call
 // on a device looks up the array's device address with cudaGetSymbolAddress
 // (with that device current) and caches it; that first call should come
-// before any stream capture.  All calls share the array: the kernels fully
-// rewrite the part they use before reading it, so nothing needs clearing,
-// but calls that overlap on the GPU (concurrent streams) race on it.
+// before any stream capture.  All calls share the array, which keeps the last
+// call's contents.  Its head holds the per-row arrival counters the split-K
+// merge needs at zero; every call clears them (an async memset on the
+// caller's stream, no allocation) before it launches.  Calls that overlap on
+// the GPU (concurrent streams) race on the array.
 #include <mutex>
 
 #include "../../include/bsp.h"
@@ -53,6 +55,10 @@ extern "C" bsp_status bsp_sparse_pa_decode_noalloc(const bsp_kv_cache* kv, const
   }
   const int32_t group = num_q_heads / kv->num_kv_heads;
   if (bsp_sparse_pa_decode_workspace_bytes(num_rows, k_pages, group) > kScratchBytes) return BSP_ERR_WORKSPACE;
+  if (num_rows > 0 &&
+      cudaMemsetAsync(scratch, 0, bsp::sparse_pa_counter_bytes(num_rows), reinterpret_cast<cudaStream_t>(stream)) !=
+          cudaSuccess)
+    return BSP_ERR_CUDA;
   return bsp_sparse_pa_decode(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, num_rows, k_pages, sm_scale, out,
                               scratch, kScratchBytes, dev_err, stream);
 }

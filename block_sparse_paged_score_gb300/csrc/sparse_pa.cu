@@ -26,8 +26,11 @@
 // MXFP4 pages are dequantised by the warp into a bf16 page (e2m1 * 2^(e-127)
 // is exact in bf16) and then take the bf16 path.
 // The 4 warps merge in shared memory (log-sum-exp); a row with one split is
-// written directly, otherwise the CTA writes (m, l, O) to the workspace and
-// sparse_pa_merge combines the splits.
+// written directly.  Otherwise the CTA writes (m, l, O) to the workspace and
+// bumps the row's arrival counter; the CTA that arrives last merges every
+// split of the row and resets the counter to zero.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,11 +40,35 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// fp8 -> f16 of the K/V pages: the integer bit move (value * 2^-8) or the
+// hardware cvt (value * 1); the power of two is folded into the scales
+#ifndef BSP_PA_E4M3_CVT
+#define BSP_PA_E4M3_CVT 1
+#endif
+constexpr float kE4m3Fold = BSP_PA_E4M3_CVT ? 1.f : 256.f;
+__device__ __forceinline__ void kv_e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if (BSP_PA_E4M3_CVT)
+    e4m3x4_to_f16x2_cvt(w, lo, hi);
+  else
+    e4m3x4_to_f16x2_scaled(w, lo, hi);
+}
+constexpr float kRescaleLog2 = 8.f;
+
 template <int KV>
 struct PaFmt;
+// pages in flight per warp (fp8) and the split plan's target of resident
+// CTAs per SM; compile-time so that they can be tuned by measurement
+#ifndef BSP_PA_FP8_RING
+#define BSP_PA_FP8_RING 3
+#endif
+#ifndef BSP_PA_CTAS_PER_SM
+#define BSP_PA_CTAS_PER_SM 3
+#endif
+constexpr int kMaxCluster = 8;  // portable thread-block cluster size
+
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
-  static constexpr int kRing = 3, kSlot = 4096, kDeq = 0;
+  static constexpr int kRing = BSP_PA_FP8_RING, kSlot = 4096, kDeq = 0;
 };
 template <>
 struct PaFmt<BSP_BF16> {
@@ -53,19 +80,40 @@ struct PaFmt<BSP_MXFP4> {
   static constexpr int kRing = 3, kSlot = 2176, kDeq = 8192;
 };
 
+// shared memory: the rings (and MXFP4 dequant pages) during the page loop,
+// reused after it for the four warps' merge ([4][16] m, [4][16] l,
+// [4][16][136] O); the mbarriers sit after the larger of the two
+constexpr int kCombineFloats = 128 + 4 * 16 * (128 + 8);
+// plus this CTA's partial (m[16], l[16], O[16][128]) that cluster peers read
+constexpr int kCombineBytes = (kCombineFloats + 32 + 16 * 128) * 4;
 template <int KV>
-constexpr int pa_smem_bytes() {
-  return 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq + 4 * PaFmt<KV>::kRing * 8;
+__host__ __device__ constexpr int pa_bar_offset() {
+  return (4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq) > kCombineBytes
+             ? 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq
+             : kCombineBytes;
 }
-static_assert(4 * 3 * 4096 >= 4 * (16 * 128 + 32) * 4, "combine area fits the fp8 ring");
+template <int KV>
+__host__ __device__ constexpr int pa_smem_bytes() {
+  return pa_bar_offset<KV>() + 4 * PaFmt<KV>::kRing * 8;
+}
 
+// n (2 or 4) consecutive query elements starting at element `off`
+// (8-byte or 4-byte aligned for bf16, 4- or 2-byte for e4m3)
 __device__ __forceinline__ void load_q_vals(const void* q, int q_dtype, int64_t off, int n, float* v) {
   if (q_dtype == BSP_BF16) {
     const uint16_t* p = static_cast<const uint16_t*>(q) + off;
-    for (int i = 0; i < n; ++i) v[i] = bf16_bits_to_float(p[i]);
+    if (n == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+      v[0] = bf16_bits_to_float(w.x & 0xFFFF), v[1] = bf16_bits_to_float(w.x >> 16);
+      v[2] = bf16_bits_to_float(w.y & 0xFFFF), v[3] = bf16_bits_to_float(w.y >> 16);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      v[0] = bf16_bits_to_float(w & 0xFFFF), v[1] = bf16_bits_to_float(w >> 16);
+    }
   } else {
     const uint8_t* p = static_cast<const uint8_t*>(q) + off;
-    for (int i = 0; i < n; ++i) v[i] = e4m3_to_float(p[i]);
+    const uint32_t w = n == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
+    for (int i = 0; i < n; ++i) v[i] = e4m3_to_float(w >> (8 * i));
   }
 }
 
@@ -116,12 +164,19 @@ __device__ __forceinline__ void mx_page_to_bf16(const uint8_t* slot, uint8_t* dq
   }
 }
 
+// the workspace starts with one int32 arrival counter per row, padded to 256 B
+__host__ __device__ constexpr int64_t ws_counter_floats(int64_t rows) { return (rows + 63) / 64 * 64; }
+
+#ifndef BSP_PA_MIN_CTAS
+#define BSP_PA_MIN_CTAS 1
+#endif
+
 template <int KV>
-__global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
+__global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
   constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
   constexpr bool F16 = KV == BSP_FP8_E4M3;  // f16 mma with permuted tokens; else bf16
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 4 * R * SB + 4 * DQ);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>());
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int64_t cta = blockIdx.x;
@@ -145,9 +200,21 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
   uint64_t* wbar = bars + warp * R;
   uint8_t* wdq = smem + 4 * R * SB + warp * DQ;
 
-  auto issue = [&](int i) {
-    const int pg = p0 + warp + 4 * i;
-    int64_t id = sbt[pg];
+  // this warp's page ids, 32 at a time, loaded together ahead of use: lane j
+  // holds the id of the warp's page 32*c + j (the ring issues its TMA copies
+  // from these without a dependent global load)
+  int32_t my_id = 0;
+  int id_chunk = 0;
+  if (lane < nw) my_id = sbt[p0 + warp + 4 * lane];
+  auto id_of = [&](int j) -> int32_t {  // warp-uniform j
+    if ((j >> 5) != id_chunk) {
+      id_chunk = j >> 5;
+      const int jj = 32 * id_chunk + lane;
+      my_id = jj < nw ? sbt[p0 + warp + 4 * jj] : 0;
+    }
+    return __shfl_sync(0xffffffffu, my_id, j & 31);
+  };
+  auto issue = [&](int i, int64_t id) {
     if (id < 0 || id >= p.num_ids) {
       set_err(p.err, BSP_DEVERR_PAGE_ID);
       id = 0;
@@ -169,8 +236,11 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
       bulk_g2s(slot + PB, p.v_base + id * p.id_stride + static_cast<int64_t>(h) * PB, PB, bar);
     }
   };
-  if (lane == 0)
-    for (int i = 0; i < min(R, nw); ++i) issue(i);
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int32_t id = id_of(i);
+    if (lane == 0 && i < nw) issue(i, id);
+  }
 
   // Q fragments (A operand), rows = heads g and g+8 of this KV head
   uint32_t qa[8][4];
@@ -211,9 +281,12 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
     if (KV == BSP_MXFP4) {
       mx_page_to_bf16(wring + st * SB, wdq, lane);
       __syncwarp();
-      if (lane == 0 && i + R < nw) {
-        fence_proxy_async();
-        issue(i + R);
+      {
+        const int32_t id = id_of(i + R);
+        if (lane == 0 && i + R < nw) {
+          fence_proxy_async();
+          issue(i + R, id);
+        }
       }
       kaddr = smem_u32(wdq);
       vaddr = kaddr + 4096;
@@ -222,41 +295,56 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
       vaddr = kaddr + SB / 2;
     }
 
-    // S = Q Kt
+    // S = Q Kt: both 8-token n-tiles interleaved, two accumulators each, so
+    // no mma waits on the one before it for more than 4 steps
     float s[2][4];
+    {
+      float acc[2][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) acc[nt][e][0] = acc[nt][e][1] = acc[nt][e][2] = acc[nt][e][3] = 0.f;
       if (F16) {
         const int rr = lane & 7;
-        const int tok = 4 * (rr >> 1) + 2 * nt + (rr & 1);
 #pragma unroll
         for (int q4 = 0; q4 < 2; ++q4) {
-          uint32_t r[4];
-          ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + tok * 16);
+          uint32_t r[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const int tok = 4 * (rr >> 1) + 2 * nt + (rr & 1);
+            ldsm_x4(r[nt][0], r[nt][1], r[nt][2], r[nt][3], kaddr + (4 * q4 + (lane >> 3)) * 256 + tok * 16);
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            uint32_t b0, b1;
-            e4m3x4_to_f16x2_scaled(r[j], b0, b1);
             const int kc = 4 * q4 + j;
-            mma_f16(acc, qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              uint32_t b0, b1;
+              kv_e4m3x4_to_f16x2(r[nt][j], b0, b1);
+              mma_f16(acc[nt][j & 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+            }
           }
         }
       } else {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t r[4];
-          ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + (8 * nt + (lane & 7)) * 16);
           const int kc = 2 * q4;
-          mma_bf16(acc, qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], r[0], r[1]);
-          mma_bf16(acc, qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], r[2], r[3]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t r[4];
+            ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + (8 * nt + (lane & 7)) * 16);
+            mma_bf16(acc[nt][0], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], r[0], r[1]);
+            mma_bf16(acc[nt][1], qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], r[2], r[3]);
+          }
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
-        s[nt][j] = pg * kPage + tok < ctx ? acc[j] * qk_scale : -INFINITY;
-      }
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
+          s[nt][j] = pg * kPage + tok < ctx ? (acc[nt][0][j] + acc[nt][1][j]) * qk_scale : -INFINITY;
+        }
     }
 
     // online softmax (log2 domain); rows g (regs 0,1) and g+8 (regs 2,3)
@@ -266,7 +354,12 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    // The reference max moves only when a row's max grows by more than 2^8
+    // (kRescaleLog2): P then stays below 256, exact enough in f16/bf16 and far
+    // from overflow, and O is rescaled only on the (warp-uniform) pages where
+    // some row's max moved.  softmax = exp2(s - m) / sum is the same for any m.
+    const bool move0 = mx0 > m0 + kRescaleLog2, move1 = mx1 > m1 + kRescaleLog2;
+    const float mn0 = move0 ? mx0 : m0, mn1 = move1 ? mx1 : m1;
     const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
     m0 = mn0, m1 = mn1;
     float pr[2][4];
@@ -279,9 +372,11 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
     }
     l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
     l1 = l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+    if (__any_sync(0xffffffffu, move0 || move1)) {
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      o[nd][0] *= al0, o[nd][1] *= al0, o[nd][2] *= al1, o[nd][3] *= al1;
+      for (int nd = 0; nd < 16; ++nd) {
+        o[nd][0] *= al0, o[nd][1] *= al0, o[nd][2] *= al1, o[nd][3] *= al1;
+      }
     }
 
     // O += P V
@@ -298,7 +393,7 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t b0, b1;
-          e4m3x4_to_f16x2_scaled(r[j], b0, b1);
+          kv_e4m3x4_to_f16x2(r[j], b0, b1);
           mma_f16(o[4 * q4 + j], pa0, pa1, pa2, pa3, b0, b1);
         }
       }
@@ -321,9 +416,12 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
       }
     }
     __syncwarp();
-    if (KV != BSP_MXFP4 && lane == 0 && i + R < nw) {
-      fence_proxy_async();
-      issue(i + R);
+    if (KV != BSP_MXFP4) {
+      const int32_t id = id_of(i + R);
+      if (lane == 0 && i + R < nw) {
+        fence_proxy_async();
+        issue(i + R, id);
+      }
     }
   }
 
@@ -333,22 +431,25 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // merge the four warps in shared memory (the rings are no longer used)
+  // merge the four warps in shared memory (the rings are no longer used);
+  // rows padded to 136 floats so the fragment stores hit each bank twice at most
+  constexpr int kCo = kDim + 8;
   __syncthreads();
   float* cm = reinterpret_cast<float*>(smem);  // [4][16]
   float* cl = cm + 64;                         // [4][16]
-  float* co = cl + 64;                         // [4][16][128]
+  float* co = cl + 64;                         // [4][16][kCo]
   if (t == 0) {
     cm[warp * 16 + g] = m0, cm[warp * 16 + g + 8] = m1;
     cl[warp * 16 + g] = l0, cl[warp * 16 + g + 8] = l1;
   }
 #pragma unroll
   for (int nd = 0; nd < 16; ++nd) {
-    *reinterpret_cast<float2*>(co + (warp * 16 + g) * kDim + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
-    *reinterpret_cast<float2*>(co + (warp * 16 + g + 8) * kDim + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
+    *reinterpret_cast<float2*>(co + (warp * 16 + g) * kCo + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+    *reinterpret_cast<float2*>(co + (warp * 16 + g + 8) * kCo + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
   }
   __syncthreads();
-  const int hh = tid >> 3, d0 = (tid & 7) * 16;
+  // thread -> head hh, dims 4*(tid%8) + 32*j (j < 4): 128 contiguous bytes per 8 lanes
+  const int hh = tid >> 3, dq = 4 * (tid & 7);
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 16 + hh]);
@@ -358,62 +459,110 @@ __global__ void __launch_bounds__(128) sparse_pa_kernel(SparsePaParams p, float 
     wgt[w] = M == -INFINITY ? 0.f : exp2f(cm[w * 16 + hh] - M);
     L += wgt[w] * cl[w * 16 + hh];
   }
-  float acc[16];
+  float4 acc[4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float a = 0.f;
+  for (int j = 0; j < 4; ++j) {
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) a += wgt[w] * co[(w * 16 + hh) * kDim + d0 + j];
-    acc[j] = a;
+    for (int w = 0; w < 4; ++w) {
+      const float4 c = *reinterpret_cast<const float4*>(co + (w * 16 + hh) * kCo + dq + 32 * j);
+      acc[j].x += wgt[w] * c.x, acc[j].y += wgt[w] * c.y, acc[j].z += wgt[w] * c.z, acc[j].w += wgt[w] * c.w;
+    }
   }
+  uint16_t* orow = static_cast<uint16_t*>(p.out) + (token * hq + static_cast<int64_t>(h) * p.group + hh) * kDim;
   if (p.nsplit == 1) {
     if (hh < p.group) {
       const float f = L > 0.f ? out_scale / L : 0.f;
-      uint32_t w[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(acc[2 * j] * f, acc[2 * j + 1] * f);
-      uint16_t* dst = static_cast<uint16_t*>(p.out) + (token * hq + static_cast<int64_t>(h) * p.group + hh) * kDim + d0;
-      reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(orow + dq + 32 * j) =
+            make_uint2(pack_bf16x2(acc[j].x * f, acc[j].y * f), pack_bf16x2(acc[j].z * f, acc[j].w * f));
     }
-  } else {
-    const int64_t unit = static_cast<int64_t>(row) * p.nsplit + split;
-    float* wo = p.ws + (unit * 16 + hh) * kDim + d0;
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(wo + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-    if ((tid & 7) == 0) {
-      float* wml = p.ws + static_cast<int64_t>(p.num_rows) * p.nsplit * 16 * kDim + (unit * 16 + hh) * 2;
-      wml[0] = M;
-      wml[1] = L;
-    }
+    return;
   }
-}
 
-// combine the splits of a row: one CTA per row, thread = dim
-__global__ void __launch_bounds__(128) sparse_pa_merge_kernel(SparsePaParams p, float out_scale) {
-  const int row = blockIdx.x, d = threadIdx.x;
-  const int h = row % p.hkv;
-  const int64_t token = row / p.hkv;
-  const int hq = p.hkv * p.group;
-  const float* ml = p.ws + static_cast<int64_t>(p.num_rows) * p.nsplit * 16 * kDim;
-  for (int hh = 0; hh < p.group; ++hh) {
-    float M = -INFINITY;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, ml[((static_cast<int64_t>(row) * p.nsplit + s) * 16 + hh) * 2]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < p.nsplit; ++s) {
-        const int64_t unit = static_cast<int64_t>(row) * p.nsplit + s;
-        const float m = ml[(unit * 16 + hh) * 2];
-        if (m == -INFINITY) continue;
-        const float w = exp2f(m - M);
-        L += w * ml[(unit * 16 + hh) * 2 + 1];
-        O += w * p.ws[(unit * 16 + hh) * kDim + d];
+  if (p.cluster > 1) {
+    // The row's splits form one thread-block cluster: publish this split's
+    // partial in shared memory, and after a cluster barrier CTA k merges
+    // heads k, k+nsplit, ... reading every peer's partial through
+    // distributed shared memory (no global round trip).
+    float* pm = cm + kCombineFloats;  // [16]
+    float* pl = pm + 16;              // [16]
+    float* po = pl + 16;              // [16][128]
+    if ((tid & 7) == 0) pm[hh] = M, pl[hh] = L;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(po + hh * kDim + dq + 32 * j) = acc[j];
+    cluster_sync();
+    const uint32_t rank = cluster_ctarank();
+    for (int head = static_cast<int>(rank); head < p.group; head += p.nsplit) {
+      float Mx = -INFINITY;
+      for (int sp = 0; sp < p.nsplit; ++sp) Mx = fmaxf(Mx, ld_dsmem_f32(pm + head, sp));
+      float Ls = 0.f, O = 0.f;
+      for (int sp = 0; sp < p.nsplit; ++sp) {
+        const float m = ld_dsmem_f32(pm + head, sp);
+        const float w = (Mx == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - Mx);
+        Ls += w * ld_dsmem_f32(pl + head, sp);
+        O += w * ld_dsmem_f32(po + head * kDim + tid, sp);
+      }
+      static_cast<__nv_bfloat16*>(p.out)[(token * hq + static_cast<int64_t>(h) * p.group + head) * kDim + tid] =
+          __float2bfloat16_rn(Ls > 0.f ? O * (out_scale / Ls) : 0.f);
+    }
+    cluster_sync();  // peers are done reading this CTA's shared memory
+    return;
+  }
+
+  // split-K: publish this split's (m, l, O), then the last CTA of the row to
+  // arrive merges all splits (no second kernel, no waiting: the counter tells
+  // the last one that every other split has been written)
+  int32_t* counters = reinterpret_cast<int32_t*>(p.ws);
+  float* wso = p.ws + ws_counter_floats(p.num_rows);
+  float* wsml = wso + static_cast<int64_t>(p.num_rows) * p.nsplit * 16 * kDim;
+  const int64_t unit = static_cast<int64_t>(row) * p.nsplit + split;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(wso + (unit * 16 + hh) * kDim + dq + 32 * j) = acc[j];
+  if ((tid & 7) == 0) *reinterpret_cast<float2*>(wsml + (unit * 16 + hh) * 2) = make_float2(M, L);
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) s_last = atomicAdd(&counters[row], 1) == p.nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float* sw = cm;  // [nsplit][16] merge weights, then [16] 1/L
+  float* sinv = cm + 16 * p.nsplit;
+  if (tid < 16) {
+    float Mx = -INFINITY;
+    for (int sp = 0; sp < p.nsplit; ++sp)
+      Mx = fmaxf(Mx, __ldcg(wsml + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + tid) * 2));
+    float Ls = 0.f;
+    for (int sp = 0; sp < p.nsplit; ++sp) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(wsml + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + tid) * 2));
+      const float w = (Mx == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
+      sw[sp * 16 + tid] = w;
+      Ls += w * ml.y;
+    }
+    sinv[tid] = Ls > 0.f ? out_scale / Ls : 0.f;
+  }
+  __syncthreads();
+  if (hh < p.group) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < p.nsplit; ++sp) {
+      const float w = sw[sp * 16 + hh];
+      const float* src = wso + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + hh) * kDim + dq;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 c = __ldcg(reinterpret_cast<const float4*>(src + 32 * j));
+        acc[j].x += w * c.x, acc[j].y += w * c.y, acc[j].z += w * c.z, acc[j].w += w * c.w;
       }
     }
-    const float v = L > 0.f ? O * (out_scale / L) : 0.f;
-    reinterpret_cast<__nv_bfloat16*>(p.out)[(token * hq + static_cast<int64_t>(h) * p.group + hh) * kDim + d] =
-        __float2bfloat16_rn(v);
+    const float f = sinv[hh];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint2*>(orow + dq + 32 * j) =
+          make_uint2(pack_bf16x2(acc[j].x * f, acc[j].y * f), pack_bf16x2(acc[j].z * f, acc[j].w * f));
   }
+  if (tid == 0) counters[row] = 0;  // ready for the next call
 }
 
 template <int KV>
@@ -425,26 +574,43 @@ cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * 256.f : 1.f;
-  const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * 256.f : 1.f;
+  const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * kE4m3Fold : 1.f;
+  const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * kE4m3Fold : 1.f;
   const float qk_scale = p.sm_scale * kfold * kLog2e;
   const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
-  sparse_pa_kernel<KV><<<static_cast<unsigned>(ctas), 128, bytes, s>>>(p, qk_scale, vfold);
-  ++*launches;
-  cudaError_t e = cudaPeekAtLastError();
-  if (e != cudaSuccess || p.nsplit == 1) return e;
-  sparse_pa_merge_kernel<<<p.num_rows, 128, 0, s>>>(p, vfold);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (p.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_pa_kernel<KV>, p, qk_scale, vfold);
+  if (e != cudaSuccess) return e;
   ++*launches;
   return cudaPeekAtLastError();
 }
 
 }  // namespace
 
-void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split) {
-  int64_t rows = num_rows > 0 ? num_rows : 1;
-  int64_t ns = (4LL * num_sms + rows - 1) / rows;
-  const int64_t max_ns = (k_pages + 3) / 4;
+void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split,
+                    int32_t* cluster) {
+  // aim at one wave of about BSP_PA_CTAS_PER_SM resident CTAs per SM; split
+  // a row over up to 8 CTAs (one cluster, merged on chip) when that still
+  // covers the GPU, over more (merged through the workspace) only for very
+  // few rows
+  const int64_t rows = num_rows > 0 ? num_rows : 1;
+  int64_t ns = (static_cast<int64_t>(BSP_PA_CTAS_PER_SM) * num_sms + rows - 1) / rows;
+  const int64_t max_ns = std::min<int64_t>(64, (k_pages + 3) / 4);
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
+  if (ns > kMaxCluster && rows * kMaxCluster >= num_sms) ns = kMaxCluster;
   int64_t pps = (k_pages + ns - 1) / ns;
   pps = (pps + 3) / 4 * 4;
   if (pps < 4) pps = 4;
@@ -452,12 +618,16 @@ void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsp
   if (ns < 1) ns = 1;
   *nsplit = static_cast<int32_t>(ns);
   *pages_per_split = static_cast<int32_t>(pps);
+  *cluster = (ns >= 2 && ns <= kMaxCluster) ? static_cast<int32_t>(ns) : 0;
 }
 
 size_t sparse_pa_ws_bytes(int32_t num_rows, int32_t nsplit) {
-  if (nsplit <= 1) return 0;
-  return static_cast<size_t>(num_rows) * nsplit * 16 * (kDim + 2) * sizeof(float);
+  if (nsplit <= kMaxCluster) return 0;  // no split, or merged on chip in a cluster
+  return (static_cast<size_t>(ws_counter_floats(num_rows)) + static_cast<size_t>(num_rows) * nsplit * 16 * (kDim + 2)) *
+         sizeof(float);
 }
+
+size_t sparse_pa_counter_bytes(int32_t num_rows) { return static_cast<size_t>(ws_counter_floats(num_rows)) * 4; }
 
 cudaError_t launch_sparse_pa(const SparsePaParams& p, cudaStream_t s, int* launches) {
   if (p.num_rows == 0) return cudaSuccess;

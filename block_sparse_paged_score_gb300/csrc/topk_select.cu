@@ -4,7 +4,8 @@
 // tail page is always selected"; vLLM API docs of
 // MiniMaxM3SparseAiterPAMetadataBuilder: the page-16 rebase B*16 + j).
 //
-// One CTA of 512 threads per row.  Scores become order-preserving uint32
+// Rows of up to 2048 pages: one warp per row (topk_warp_kernel).  Longer
+// rows: one CTA of 512 threads per row.  Scores become order-preserving uint32
 // keys (-0 folded onto +0) kept in shared memory.  A most-significant-digit
 // radix select (four 8-bit passes, shared-memory histograms, one warp scans
 // the 256 bins) finds the k'-th largest key tau and how many keys equal to
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
   const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
   {
     int eqr = eq_before, pos = sel_before;
+    int cur_blk = -1, cur_id = 0;  // this thread's pages are contiguous: few distinct blocks
     for (int i = b; i < e; ++i) {
       bool sel = !none;
       if (radix) {
@@ -173,8 +175,12 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
         eqr += k == tau;
       }
       if (sel && pos < need) {  // exactly `need` are selected; the bound keeps writes in the row
+        if (i / kPagesPerSide != cur_blk) {
+          cur_blk = i / kPagesPerSide;
+          cur_id = p.block_table[bt_row + cur_blk] * p.id_mul;
+        }
         ti[pos] = i;
-        bt[pos] = p.block_table[bt_row + i / kPagesPerSide] * p.id_mul + i % kPagesPerSide;
+        bt[pos] = cur_id + i % kPagesPerSide;
         ++pos;
       }
     }
@@ -194,10 +200,117 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
   }
 }
 
+// One warp per row for rows of up to 32*KPL candidates, four rows per CTA.
+// Lane l holds the keys of pages l, l+32, ... in registers.  The k'-th key
+// tau is built bit by bit from the top (keep a bit when at least `need` keys
+// are >= the prefix with that bit set; one warp reduction per bit).  Pages
+// are then visited in page order, 32 at a time: ballots give each page its
+// rank among the keys equal to tau (the lower page wins a tie) and its output
+// slot, so the table is emitted ascending with no sort and no block barrier.
+template <int KPL>
+__global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
+  __shared__ int32_t s_bt[4][(32 * KPL + kPagesPerSide - 1) / kPagesPerSide];
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (r >= p.num_rows) return;
+  int32_t* wbt = s_bt[threadIdx.x >> 5];
+  const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
+  const int max_len = p.max_pages * kPage;
+  // independent loads first: the row's length and sequence, every score of
+  // the row and its block ids (valid memory whatever the length)
+  const int L = min(max(p.row_len[r], 0), max_len);
+  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
+  float sv[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) sv[i] = lane + 32 * i < p.max_pages ? srow[lane + 32 * i] : 0.f;
+  for (int b = lane; b < (p.max_pages + kPagesPerSide - 1) / kPagesPerSide; b += 32)
+    wbt[b] = p.block_table[bt_row + b] * p.id_mul;
+  __syncwarp();
+  const int n = (L + kPage - 1) / kPage;
+  const int kk = min(p.k_pages, n);
+  int32_t* ti = p.topk_idx + static_cast<int64_t>(r) * p.k_pages;
+  int32_t* bt = p.sparse_bt + static_cast<int64_t>(r) * p.k_pages;
+  for (int m = kk + lane; m < p.k_pages; m += 32) ti[m] = bt[m] = -1;
+  if (kk == 0) {
+    if (lane == 0) p.sparse_ctx[r] = 0;
+    return;
+  }
+  const int n_cand = p.force_tail ? n - 1 : n;
+  const int need = p.force_tail ? kk - 1 : kk;
+  const bool all = need >= n_cand, none = need == 0, radix = !all && !none;
+  uint32_t key[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int pg = lane + 32 * i;
+    key[i] = (radix && pg < n_cand) ? order_key(sv[i]) : 0u;
+  }
+  uint32_t tau = 0;
+  int take_eq = 0;
+  if (radix) {
+    // keys of real candidates are > 0 (order_key(-inf) = 0x007fffff), padding is 0
+    uint32_t prefix = 0;
+    for (int b = 31; b >= 0; --b) {
+      const uint32_t cand = prefix | (1u << b);
+      unsigned c = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) c += key[i] >= cand;
+      if (static_cast<int>(__reduce_add_sync(full, c)) >= need) prefix = cand;
+    }
+    tau = prefix;
+    unsigned gt = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) gt += key[i] > tau;
+    take_eq = need - static_cast<int>(__reduce_add_sync(full, gt));
+  }
+  int base = 0, eq_base = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    if (32 * i >= n_cand) break;
+    const int pg = lane + 32 * i;
+    const bool valid = pg < n_cand;
+    const bool eq = radix && valid && key[i] == tau;
+    const unsigned beq = __ballot_sync(full, eq);
+    const int eq_rank = eq_base + __popc(beq & lt);
+    const bool sel = valid && !none && (all || key[i] > tau || (eq && eq_rank < take_eq));
+    const unsigned bsel = __ballot_sync(full, sel);
+    const int pos = base + __popc(bsel & lt);
+    if (sel && pos < need) {
+      ti[pos] = pg;
+      bt[pos] = wbt[pg / kPagesPerSide] + pg % kPagesPerSide;
+    }
+    base += __popc(bsel);
+    eq_base += __popc(beq);
+  }
+  if (lane == 0) {
+    const int tail_len = L - kPage * (n - 1);
+    if (p.force_tail) {
+      const int pg = n - 1;
+      ti[kk - 1] = pg;
+      bt[kk - 1] = wbt[pg / kPagesPerSide] + pg % kPagesPerSide;
+      p.sparse_ctx[r] = kPage * (kk - 1) + tail_len;
+    }
+  }
+  if (!p.force_tail) {
+    __syncwarp();
+    if (lane == 0) p.sparse_ctx[r] = kPage * (kk - 1) + (ti[kk - 1] == n - 1 ? L - kPage * (n - 1) : kPage);
+  }
+}
+
+template <int KPL>
+cudaError_t launch_warp(const TopkParams& p, cudaStream_t s) {
+  topk_warp_kernel<KPL><<<(p.num_rows + 3) / 4, 128, 0, s>>>(p);
+  return cudaPeekAtLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
+  if (p.max_pages <= 128) return launch_warp<4>(p, s);
+  if (p.max_pages <= 512) return launch_warp<16>(p, s);
+  if (p.max_pages <= 1024) return launch_warp<32>(p, s);
+  if (p.max_pages <= 2048) return launch_warp<64>(p, s);
   const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
   const size_t bytes = static_cast<size_t>(cand) * 4;
   static bool configured = false;

@@ -267,8 +267,13 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
  *   token m < sparse_ctx[r] of row r is token m%16 of page sparse_bt[r, m/16]
  *   out      bf16 [tokens, Hkv*G, 128] = softmax(sm_scale * q K^T) V; rows
  *            with sparse_ctx 0 get zeros
- * Split-K over pages across CTAs, then an LSE merge kernel.  `ws` is a
- * device workspace of at least bsp_sparse_pa_decode_workspace_bytes().
+ * Split-K over pages across CTAs; the last CTA of a row to finish merges the
+ * row's splits (log-sum-exp).  `ws` is a device workspace of at least
+ * bsp_sparse_pa_decode_workspace_bytes(); it holds per-row arrival counters
+ * that must be ZERO before the first call (e.g. cudaMemset once after
+ * allocation).  Every call leaves them zero again, so a workspace is zeroed
+ * once, not per call.  Calls that overlap on the GPU need separate
+ * workspaces.
  * ---------------------------------------------------------------------- */
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group);
 bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
@@ -292,8 +297,11 @@ bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q
  *  - The first call on a device looks up the array's address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
- *  - Calls share the array: calls that overlap on the GPU (other streams,
- *    other host threads) race on it and must be serialised by the caller.
+ *  - Calls share the array and it keeps the last call's contents; each call
+ *    first clears the part that must start at zero (the split-K arrival
+ *    counters, an async memset on `stream`).  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on it and must be serialised
+ *    by the caller.
  *  - It calls no allocator (no cudaMalloc / cudaFree).  Arguments and errors
  *    are those of bsp_sparse_pa_decode.
  * ---------------------------------------------------------------------- */

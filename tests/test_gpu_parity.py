@@ -126,11 +126,13 @@ def test_topk_bit_exact_on_oracle_scores(bsp, name):
     assert np.array_equal(gctx.cpu().numpy(), ctx)
 
 
+@pytest.mark.parametrize("max_pages", [100, 700, 2048, 3000])
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
-def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype):
+def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
+    """Both selectors: one warp per row up to 2048 pages, one CTA per row beyond."""
     rng = np.random.default_rng(3)
-    rows, max_pages = 300, 700
+    rows = 300
     sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
     sc[::5] = rng.standard_normal((len(sc[::5]), max_pages)).astype(np.float32)
     sc[7, ::3] = -0.0
@@ -168,6 +170,30 @@ def test_attention_on_oracle_table(bsp, name, prefill):
     # rows with nothing to attend are exactly zero
     z = np.repeat(ctx == 0, w.group)
     assert (got[z] == 0).all()
+
+
+@pytest.mark.parametrize("name", ["fp8", "mx", "bf16"])
+def test_attention_split_merge_paths(bsp, name):
+    """Two ways a split decode row is finished: a cluster of up to 8 split
+    CTAs merged through distributed shared memory, and more splits merged
+    through the workspace (very few rows, wide selections).  One CTA per
+    row, the third way, is the prefill call's path and covered above."""
+    for k_pages, rows in ((16, None), (128, None), (128, 2)):
+        w = W.Workload(dict(MINI[name], k_pages=k_pages))
+        o, g = OracleSide(w), GpuSide(w)
+        ti, sb, ctx = o.topk(o.scores())
+        n = w.num_rows if rows is None else rows
+        sel = np.arange(w.num_rows - n, w.num_rows)  # the longest rows
+        ref = bf16_f32(torch.from_numpy(o.attention(sb, ctx).view(np.int16))).reshape(w.num_rows, w.group, 128)[sel]
+        q = g.q.reshape(w.num_tokens, w.hq, 128)[w.num_tokens - n // w.hkv:].contiguous()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = bsp.sparse_pa_decode(g.kv, q, w.q_dtype, w.hq, torch.from_numpy(sb[sel]).cuda(),
+                                   torch.from_numpy(ctx[sel]).cuda(), w.k_pages, SM_SCALE, dev_err=err)
+        got = bf16_f32(out).reshape(n, w.group, 128)
+        assert err.item() == 0
+        ok, worst, rl2 = attention_close(got, ref)
+        print(f"{name} k={k_pages} rows={n} ws={bsp.decode_workspace_bytes(n, k_pages, w.group)}: {worst:.3g} {rl2:.3g}")
+        assert ok, (k_pages, n, worst, rl2)
 
 
 @pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx"])
@@ -256,7 +282,11 @@ def test_host_argument_errors(bsp):
         bsp.sparse_pa_decode(g.kv, g.q[:, :12].contiguous(), w.q_dtype, 12, torch.from_numpy(sb).cuda(),
                              torch.from_numpy(ctx).cuda(), w.k_pages)
     assert e.value.status == 2
-    with pytest.raises(bsp.BspError) as e:  # workspace too small
-        bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb).cuda(), torch.from_numpy(ctx).cuda(),
-                             w.k_pages, ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    # a wide selection over few rows merges through the workspace: too small a one is refused
+    sb128 = np.full((sb.shape[0], 128), -1, np.int32)
+    sb128[:, :sb.shape[1]] = sb
+    assert bsp.decode_workspace_bytes(sb.shape[0], 128, w.group) > 16
+    with pytest.raises(bsp.BspError) as e:
+        bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb128).cuda(), torch.from_numpy(ctx).cuda(),
+                             128, ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 3

@@ -11,7 +11,9 @@ import numpy as np
 import pytest
 import torch
 
-from harness import SM_SCALE, GpuSide, OracleSide, attention_close, bf16_f32, mini
+from block_sparse_paged_score_gb300 import workloads as W
+
+from harness import MINI, SM_SCALE, GpuSide, OracleSide, attention_close, bf16_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +27,9 @@ def _call_noalloc(bsp, kv, q, q_dtype, hq, sbt, ctx, k_pages, out, err):
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
     from block_sparse_paged_score_gb300 import bsp
     for name in ("fp8", "mx"):
-        w = mini(name)
+        # few rows and a wide selection: the plan splits rows over more CTAs
+        # than one cluster holds, so the partials go through the scratch
+        w = W.Workload(dict(MINI[name], k_pages=128))
         o, g = OracleSide(w), GpuSide(w)
         ti, sb, ctx = o.topk(o.scores())
         assert bsp.decode_workspace_bytes(w.num_rows, w.k_pages, w.group) > 0  # the scratch is used
