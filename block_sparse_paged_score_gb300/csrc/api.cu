@@ -290,9 +290,7 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group) {
   (void)group;
   if (num_rows <= 0 || k_pages <= 0) return 0;
-  int32_t ns, pps, cl;
-  sparse_pa_plan(num_rows, k_pages, device_sms(), &ns, &pps, &cl);
-  return sparse_pa_ws_bytes(num_rows, ns);
+  return sparse_pa_ws_bytes(num_rows, sparse_pa_plan(num_rows, k_pages, device_sms()));
 }
 
 static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
@@ -328,8 +326,12 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   p.out = out;
   p.err = dev_err;
   if (decode) {
-    sparse_pa_plan(num_rows, k_pages, device_sms(), &p.nsplit, &p.pages_per_split, &p.cluster);
-    const size_t need = sparse_pa_ws_bytes(num_rows, p.nsplit);
+    const PaPlan plan = sparse_pa_plan(num_rows, k_pages, device_sms());
+    p.nsplit = plan.nsplit;
+    p.pages_per_split = plan.pages_per_split;
+    p.cluster = plan.cluster;
+    p.stream_ctas = plan.stream_ctas;
+    const size_t need = sparse_pa_ws_bytes(num_rows, plan);
     if (need) {
       if (!ws || ws_bytes < need || !al(ws, 16)) return BSP_ERR_WORKSPACE;
       p.ws = static_cast<float*>(ws);

@@ -59,6 +59,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// plain arrival (no transaction bytes): completes a phase that no copy fills
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 // Bounded wait on a phase; returns false (and flags the error) on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
@@ -202,6 +206,16 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
   return v;
 }
+
+// ---- programmatic dependent launch -----------------------------------------
+// Kernels are launched with programmatic stream serialization, so one may
+// start while the kernel before it on the stream is still running.  Each
+// kernel calls pdl_wait() before its first global-memory access: it returns
+// once the previous grid has completed and its writes are visible (at once
+// when there is no such grid).  pdl_trigger() lets the next kernel's CTAs be
+// scheduled as this grid's CTAs retire.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

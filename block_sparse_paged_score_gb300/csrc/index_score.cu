@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   const int ntok = min(p.q_group, p.num_tokens - tok0);
   const int max_len = p.max_pages * kPage;
 
+  pdl_wait();  // row lengths come from the kernel before
+  pdl_trigger();
   if (tid < 8) {
     int L = 0, r = -1;
     if (tid < ntok) {
@@ -310,8 +312,8 @@ cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  index_score_kernel<KEY><<<grid, 128, smem_bytes<KEY>(p.stages), s>>>(p);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(index_score_kernel<KEY>, grid, dim3(128), smem_bytes<KEY>(p.stages), s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 template <int KEY>

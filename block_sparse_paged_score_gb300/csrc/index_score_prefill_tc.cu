@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = blockIdx.y * kKeyBlocksPerCta;
   const int rows_per_block = static_cast<int>(p.block_stride / 128);
 
+  pdl_wait();  // queries and row lengths come from earlier kernels
+  pdl_trigger();
   if (tid == 0) {
     // locate this tile: chunks in order, ceil(size/128) tiles each
     int t = blockIdx.x, tok0 = -1, tok1 = -1;
@@ -358,8 +360,9 @@ cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t
   const int max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
   const dim3 grid(static_cast<unsigned>(p.max_tiles),
                   static_cast<unsigned>((max_blocks + kKeyBlocksPerCta - 1) / kKeyBlocksPerCta));
-  index_score_prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, p, static_cast<int32_t>(key_rows));
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(index_score_prefill_kernel, grid, dim3(kThreads), kSmemBytes, s, 0, tq, tk, p,
+                                      static_cast<int32_t>(key_rows));
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace bsp

@@ -8,6 +8,40 @@
 
 namespace bsp {
 
+// Every kernel of the library goes through this launch: programmatic stream
+// serialization (the kernel may be scheduled while the previous kernel on the
+// stream drains; it waits on griddepcontrol before touching global memory)
+// and, for cluster > 1, a 1-D thread-block cluster of that size.
+#ifndef BSP_PDL
+#define BSP_PDL 1
+#endif
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (BSP_PDL) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct KvWriteParams {
   int32_t kv_dtype, hkv;
   uint8_t* k_base;
@@ -89,15 +123,19 @@ struct SparsePaParams {
   int32_t num_rows, k_pages;
   float sm_scale;
   void* out;
-  float* ws;  // partials when nsplit > 8 (not clustered)
+  float* ws;  // partials: page-balanced plan, or nsplit > 8 (not clustered)
   int32_t nsplit, pages_per_split;
-  int32_t cluster;  // 2..8: the row's splits form a cluster and merge on chip
+  int32_t cluster;      // 2..8: the row's splits form a cluster and merge on chip
+  int32_t stream_ctas;  // > 0: page-balanced persistent grid of this many CTAs
   int32_t* err;
 };
-// split plan shared by the launcher and the workspace query
-void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split,
-                    int32_t* cluster);
-size_t sparse_pa_ws_bytes(int32_t num_rows, int32_t nsplit);
+// decode plan shared by the launcher and the workspace query: either the
+// page-balanced grid (stream_ctas > 0) or per-row splits
+struct PaPlan {
+  int32_t nsplit, pages_per_split, cluster, stream_ctas;
+};
+PaPlan sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms);
+size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan);
 // bytes of the per-row arrival counters at the start of the workspace
 size_t sparse_pa_counter_bytes(int32_t num_rows);
 cudaError_t launch_sparse_pa(const SparsePaParams& p, cudaStream_t s, int* launches);

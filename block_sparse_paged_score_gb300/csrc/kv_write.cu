@@ -126,7 +126,11 @@ __device__ __forceinline__ void kv_page_write_block(const KvWriteParams& p, int6
   }
 }
 
-__global__ void __launch_bounds__(128) kv_page_write_kernel(KvWriteParams p) { kv_page_write_block(p, blockIdx.x); }
+__global__ void __launch_bounds__(128) kv_page_write_kernel(KvWriteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  kv_page_write_block(p, blockIdx.x);
+}
 
 // 8 elements per thread, 128 threads per block
 __device__ __forceinline__ void cast_e4m3_block(const uint16_t* __restrict__ x, uint8_t* __restrict__ out, int64_t n,
@@ -150,6 +154,8 @@ __device__ __forceinline__ void cast_e4m3_block(const uint16_t* __restrict__ x, 
 
 __global__ void __launch_bounds__(128) cast_e4m3_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ out,
                                                         int64_t n) {
+  pdl_wait();
+  pdl_trigger();
   cast_e4m3_block(x, out, n, blockIdx.x);
 }
 
@@ -170,6 +176,8 @@ __device__ __forceinline__ void row_lengths_decode_block(const int32_t* seq_lens
 __global__ void __launch_bounds__(128) row_lengths_decode_kernel(const int32_t* seq_lens, int32_t num_seqs,
                                                                  int32_t q_len, int32_t heads, int32_t* row_seq,
                                                                  int32_t* row_len) {
+  pdl_wait();
+  pdl_trigger();
   row_lengths_decode_block(seq_lens, num_seqs, q_len, heads, row_seq, row_len, blockIdx.x);
 }
 
@@ -177,6 +185,8 @@ __global__ void __launch_bounds__(128) row_lengths_decode_kernel(const int32_t* 
 // tokens, the next blocks cast the two query tensors to e4m3, the last ones
 // compute the row lengths.  The parts are independent.
 __global__ void __launch_bounds__(128) decode_prep_kernel(DecodePrepParams p) {
+  pdl_wait();
+  pdl_trigger();
   int64_t b = blockIdx.x;
   if (b < p.write_blocks) return kv_page_write_block(p.write, b);
   b -= p.write_blocks;
@@ -189,6 +199,8 @@ __global__ void __launch_bounds__(128) decode_prep_kernel(DecodePrepParams p) {
 
 __global__ void row_lengths_prefill_kernel(const int32_t* req, const int32_t* pos, int32_t n, int32_t heads,
                                            int32_t* row_seq, int32_t* row_len) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (r >= static_cast<int64_t>(n) * heads) return;
   const int64_t i = r / heads;
@@ -202,23 +214,25 @@ __global__ void row_lengths_prefill_kernel(const int32_t* req, const int32_t* po
 cudaError_t launch_kv_page_write(const KvWriteParams& p, cudaStream_t s) {
   const int64_t warps = static_cast<int64_t>(p.num_tokens) * (2 * p.hkv + p.hidx);
   if (warps == 0) return cudaSuccess;
-  kv_page_write_kernel<<<static_cast<unsigned>((warps + 3) / 4), 128, 0, s>>>(p);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(kv_page_write_kernel, dim3(static_cast<unsigned>((warps + 3) / 4)), dim3(128), 0,
+                                      s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 cudaError_t launch_cast_e4m3(const uint16_t* x, uint8_t* out, int64_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  cast_e4m3_kernel<<<static_cast<unsigned>((n + 1023) / 1024), 128, 0, s>>>(x, out, n);
-  return cudaPeekAtLastError();
+  const cudaError_t e =
+      launch_kernel(cast_e4m3_kernel, dim3(static_cast<unsigned>((n + 1023) / 1024)), dim3(128), 0, s, 0, x, out, n);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 cudaError_t launch_row_lengths_decode(const int32_t* seq_lens, int32_t num_seqs, int32_t q_len, int32_t heads,
                                       int32_t* row_seq, int32_t* row_len, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(num_seqs) * q_len * heads;
   if (rows == 0) return cudaSuccess;
-  row_lengths_decode_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, s>>>(seq_lens, num_seqs, q_len,
-                                                                                       heads, row_seq, row_len);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(row_lengths_decode_kernel, dim3(static_cast<unsigned>((rows + 127) / 128)),
+                                      dim3(128), 0, s, 0, seq_lens, num_seqs, q_len, heads, row_seq, row_len);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 cudaError_t launch_decode_prep(DecodePrepParams p, cudaStream_t s) {
@@ -227,17 +241,17 @@ cudaError_t launch_decode_prep(DecodePrepParams p, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.q_len * p.heads;
   const int64_t total = p.write_blocks + p.cast_blocks[0] + p.cast_blocks[1] + (rows + 127) / 128;
   if (total == 0) return cudaSuccess;
-  decode_prep_kernel<<<static_cast<unsigned>(total), 128, 0, s>>>(p);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(decode_prep_kernel, dim3(static_cast<unsigned>(total)), dim3(128), 0, s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 cudaError_t launch_row_lengths_prefill(const int32_t* req, const int32_t* pos, int32_t n, int32_t heads,
                                        int32_t* row_seq, int32_t* row_len, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(n) * heads;
   if (rows == 0) return cudaSuccess;
-  row_lengths_prefill_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, s>>>(req, pos, n, heads,
-                                                                                        row_seq, row_len);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(row_lengths_prefill_kernel, dim3(static_cast<unsigned>((rows + 255) / 256)),
+                                      dim3(256), 0, s, 0, req, pos, n, heads, row_seq, row_len);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace bsp

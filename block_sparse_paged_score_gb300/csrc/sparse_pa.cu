@@ -9,26 +9,37 @@
 // of an mma tile; unused rows are zero) over tokens m < sparse_ctx[r]; token
 // m is token m%16 of page sparse_bt[r, m/16].
 //
-// CTA = 4 warps = one (row, split); a split is a run of pages and warp w takes
-// pages w, w+4, ... of it.  Each warp streams its pages through a ring of
+// A CTA is 4 warps.  Each warp streams its pages through a ring of
 // shared-memory slots with 1-D TMA bulk copies (K page + V page of its head;
-// MXFP4: the 1 KB data and 64 B scales of both sides) completing on mbarriers,
-// and keeps its own online softmax.  Per 16-token page:
+// MXFP4: the 1 KB data and 64 B scales of both sides) completing on
+// mbarriers, and keeps its own online softmax.  Per 16-token page:
 //   S  = Q Kt : 2 n-tiles (8 tokens) x 8 k-steps of mma.sync m16n8k16
 //   P  = exp2(S*scale - m)   (log2 domain, running max m and sum l per head)
 //   O += P V  : 16 n-tiles (8 dims) of mma.sync m16n8k16
-// fp8 pages are converted to f16 in registers right after ldmatrix (exact:
-// value * 2^-8; the k/v scales and 2^8 are folded into the softmax scale and
-// the output scale).  For fp8 the 16 tokens of a page enter the mma in the
-// order 0,1,4,5,8,9,12,13 | 2,3,6,7,... so that the S accumulator lands as the
-// P fragment whose tokens match the V rows a ldmatrix of the dim-major V page
-// hands each thread (tokens 4t..4t+3); bf16 pages use the natural order.
-// MXFP4 pages are dequantised by the warp into a bf16 page (e2m1 * 2^(e-127)
-// is exact in bf16) and then take the bf16 path.
-// The 4 warps merge in shared memory (log-sum-exp); a row with one split is
-// written directly.  Otherwise the CTA writes (m, l, O) to the workspace and
-// bumps the row's arrival counter; the CTA that arrives last merges every
-// split of the row and resets the counter to zero.
+// fp8 pages are converted to f16 in registers right after ldmatrix (exact;
+// the k/v scales are folded into the softmax scale and the output scale).
+// For fp8 the 16 tokens of a page enter the mma in the order 0,1,4,5,8,9,
+// 12,13 | 2,3,6,7,... so that the S accumulator lands as the P fragment whose
+// tokens match the V rows a ldmatrix of the dim-major V page hands each
+// thread (tokens 4t..4t+3); bf16 pages use the natural order.  MXFP4 pages
+// are dequantised by the warp into a bf16 page (e2m1 * 2^(e-127) is exact in
+// bf16) and then take the bf16 path.  The 4 warps merge in shared memory
+// (log-sum-exp).
+//
+// Two schedules:
+//  * per-row (sparse_pa_kernel): CTA = one (row, split), warp w takes pages
+//    w, w+4, ... of the split.  One split writes the row directly; 2..8
+//    splits form a thread-block cluster and merge through distributed shared
+//    memory; more splits publish (m, l, O) to the workspace and the last CTA
+//    of the row to arrive merges them.  Prefill (one split per row) and small
+//    decode batches use it.
+//  * page-balanced (sparse_pa_stream_kernel): a persistent grid of G CTAs
+//    cuts the flat [rows x k_pages] page table into G equal contiguous
+//    ranges, so every CTA streams the same number of pages in one wave
+//    whatever the row count.  A CTA walks its range row by row; its warps
+//    keep their rings full across row boundaries.  A row that lies wholly in
+//    one range is written directly; a row cut by range ends gets one partial
+//    per range, and the last CTA to publish one merges them.
 #include <algorithm>
 
 #include "common.cuh"
@@ -59,12 +70,20 @@ struct PaFmt;
 // pages in flight per warp (fp8) and the split plan's target of resident
 // CTAs per SM; compile-time so that they can be tuned by measurement
 #ifndef BSP_PA_FP8_RING
-#define BSP_PA_FP8_RING 3
+#define BSP_PA_FP8_RING 4
 #endif
 #ifndef BSP_PA_CTAS_PER_SM
 #define BSP_PA_CTAS_PER_SM 3
 #endif
 constexpr int kMaxCluster = 8;  // portable thread-block cluster size
+// page-balanced plan: resident CTAs per SM it targets, and the fewest pages
+// per CTA (at that target) for which it is taken over the per-row plan
+#ifndef BSP_PA_STREAM_CTAS_PER_SM
+#define BSP_PA_STREAM_CTAS_PER_SM 2
+#endif
+#ifndef BSP_PA_STREAM_MIN_PAGES
+#define BSP_PA_STREAM_MIN_PAGES 16
+#endif
 
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
@@ -96,6 +115,23 @@ template <int KV>
 __host__ __device__ constexpr int pa_smem_bytes() {
   return pa_bar_offset<KV>() + 4 * PaFmt<KV>::kRing * 8;
 }
+// page-balanced kernel: rings | dequant pages | merge area | mbarriers (the
+// rings stay live across the merges, so the merge area is separate)
+template <int KV>
+__host__ __device__ constexpr int pa_stream_cb_offset() {
+  return 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq;
+}
+template <int KV>
+__host__ __device__ constexpr int pa_stream_bar_offset() {
+  return pa_stream_cb_offset<KV>() + kCombineFloats * 4;
+}
+template <int KV>
+__host__ __device__ constexpr int pa_stream_smem_bytes() {
+  return pa_stream_bar_offset<KV>() + 4 * PaFmt<KV>::kRing * 8;
+}
+// the merge weights of a cut row ([ranges][16] + [16]) live in the merge
+// area, which bounds the page-balanced grid
+constexpr int kMaxStreamCtas = (kCombineFloats - 16) / 16;
 
 // n (2 or 4) consecutive query elements starting at element `off`
 // (8-byte or 4-byte aligned for bf16, 4- or 2-byte for e4m3)
@@ -171,29 +207,291 @@ __host__ __device__ constexpr int64_t ws_counter_floats(int64_t rows) { return (
 #define BSP_PA_MIN_CTAS 1
 #endif
 
+
+
+// running state of one warp's online softmax: O (16 heads x 128 dims as 16
+// n-tiles of the mma accumulator), max m and sum l of heads g and g+8
+struct PaState {
+  float o[16][4];
+  float m0, m1, l0, l1;
+};
+
+__device__ __forceinline__ void pa_state_init(PaState& a) {
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) a.o[nd][0] = a.o[nd][1] = a.o[nd][2] = a.o[nd][3] = 0.f;
+  a.m0 = a.m1 = -INFINITY;
+  a.l0 = a.l1 = 0.f;
+}
+
+// Q fragments (A operand) of one row: tile rows = query heads g and g+8 of
+// the row's KV head, starting at element `qrow` of q
+template <int KV>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[8][4], const void* q, int q_dtype, int64_t qrow,
+                                             int group, int lane) {
+  constexpr bool F16 = KV == BSP_FP8_E4M3;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int head = g + 8 * half;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (F16) {
+        if (head < group) load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 4 * t, 4, v);
+        qa[kc][half] = pack_f16x2(v[0], v[1]);
+        qa[kc][2 + half] = pack_f16x2(v[2], v[3]);
+      } else {
+        if (head < group) {
+          load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 2 * t, 2, v);
+          load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 8 + 2 * t, 2, v + 2);
+        }
+        qa[kc][half] = pack_bf16x2(v[0], v[1]);
+        qa[kc][2 + half] = pack_bf16x2(v[2], v[3]);
+      }
+    }
+  }
+}
+
+// One 16-token page of one warp: K at shared address kaddr, V at vaddr (fp8
+// layouts for KV = fp8, bf16 layouts otherwise); tok0 = the page's first
+// token in the row, tokens >= ctx are masked.
+template <int KV>
+__device__ __forceinline__ void pa_page(PaState& a, const uint32_t (&qa)[8][4], uint32_t kaddr, uint32_t vaddr,
+                                        int tok0, int ctx, float qk_scale, int lane) {
+  constexpr bool F16 = KV == BSP_FP8_E4M3;
+  const int t = lane & 3;
+  // S = Q Kt: both 8-token n-tiles interleaved, two accumulators each, so no
+  // mma waits on the one before it for more than 4 steps
+  float s[2][4];
+  {
+    float acc[2][2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) acc[nt][e][0] = acc[nt][e][1] = acc[nt][e][2] = acc[nt][e][3] = 0.f;
+    if (F16) {
+      const int rr = lane & 7;
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4) {
+        uint32_t r[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int tok = 4 * (rr >> 1) + 2 * nt + (rr & 1);
+          ldsm_x4(r[nt][0], r[nt][1], r[nt][2], r[nt][3], kaddr + (4 * q4 + (lane >> 3)) * 256 + tok * 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kc = 4 * q4 + j;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1;
+            kv_e4m3x4_to_f16x2(r[nt][j], b0, b1);
+            mma_f16(acc[nt][j & 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int kc = 2 * q4;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t r[4];
+          ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + (8 * nt + (lane & 7)) * 16);
+          mma_bf16(acc[nt][0], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], r[0], r[1]);
+          mma_bf16(acc[nt][1], qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], r[2], r[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
+        s[nt][j] = tok0 + tok < ctx ? (acc[nt][0][j] + acc[nt][1][j]) * qk_scale : -INFINITY;
+      }
+  }
+
+  // online softmax (log2 domain); rows g (regs 0,1) and g+8 (regs 2,3)
+  float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  // The reference max moves only when a row's max grows by more than 2^8
+  // (kRescaleLog2): P then stays below 256, exact enough in f16/bf16 and far
+  // from overflow, and O is rescaled only on the (warp-uniform) pages where
+  // some row's max moved.  softmax = exp2(s - m) / sum is the same for any m.
+  const bool move0 = mx0 > a.m0 + kRescaleLog2, move1 = mx1 > a.m1 + kRescaleLog2;
+  const float mn0 = move0 ? mx0 : a.m0, mn1 = move1 ? mx1 : a.m1;
+  const float al0 = exp2f(a.m0 - mn0), al1 = exp2f(a.m1 - mn1);
+  a.m0 = mn0, a.m1 = mn1;
+  float pr[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    pr[nt][0] = exp2f(s[nt][0] - mn0);
+    pr[nt][1] = exp2f(s[nt][1] - mn0);
+    pr[nt][2] = exp2f(s[nt][2] - mn1);
+    pr[nt][3] = exp2f(s[nt][3] - mn1);
+  }
+  a.l0 = a.l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
+  a.l1 = a.l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
+  if (__any_sync(0xffffffffu, move0 || move1)) {
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      a.o[nd][0] *= al0, a.o[nd][1] *= al0, a.o[nd][2] *= al1, a.o[nd][3] *= al1;
+    }
+  }
+
+  // O += P V
+  uint32_t pa0, pa1, pa2, pa3;
+  if (F16) {
+    pa0 = pack_f16x2(pr[0][0], pr[0][1]);
+    pa1 = pack_f16x2(pr[0][2], pr[0][3]);
+    pa2 = pack_f16x2(pr[1][0], pr[1][1]);
+    pa3 = pack_f16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t r[4];
+      ldsm_x4(r[0], r[1], r[2], r[3], vaddr + (8 * (4 * q4 + (lane >> 3)) + (lane & 7)) * 16);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t b0, b1;
+        kv_e4m3x4_to_f16x2(r[j], b0, b1);
+        mma_f16(a.o[4 * q4 + j], pa0, pa1, pa2, pa3, b0, b1);
+      }
+    }
+  } else {
+    // bf16 P carries 8 significant bits; P = hi + lo (both bf16) keeps ~16
+    uint32_t lo0, lo1, lo2, lo3;
+    split_bf16x2(pr[0][0], pr[0][1], pa0, lo0);
+    split_bf16x2(pr[0][2], pr[0][3], pa1, lo1);
+    split_bf16x2(pr[1][0], pr[1][1], pa2, lo2);
+    split_bf16x2(pr[1][2], pr[1][3], pa3, lo3);
+#pragma unroll
+    for (int q8 = 0; q8 < 8; ++q8) {
+      uint32_t r[4];
+      ldsm_x4(r[0], r[1], r[2], r[3],
+              vaddr + ((lane >> 3) & 1) * 2048 + (8 * (2 * q8 + (lane >> 4)) + (lane & 7)) * 16);
+      mma_bf16(a.o[2 * q8], pa0, pa1, pa2, pa3, r[0], r[1]);
+      mma_bf16(a.o[2 * q8], lo0, lo1, lo2, lo3, r[0], r[1]);
+      mma_bf16(a.o[2 * q8 + 1], pa0, pa1, pa2, pa3, r[2], r[3]);
+      mma_bf16(a.o[2 * q8 + 1], lo0, lo1, lo2, lo3, r[2], r[3]);
+    }
+  }
+}
+
+// The four warps' states of one row merged through the shared-memory area
+// cb (kCombineFloats floats; free on entry).  On return thread tid holds, for
+// head hh = tid/8 and dims dq + 32j (dq = 4*(tid%8), j < 4), the merged max
+// M (log2 domain), sum L and unnormalised output acc.  Rows are padded to 136
+// floats so the fragment stores hit each bank twice at most.
+__device__ __forceinline__ void pa_combine(float* cb, const PaState& a, int tid, float& M, float& L,
+                                           float4 (&acc)[4]) {
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  // sum l over the quad (the 4 threads of a head row)
+  float l0 = a.l0, l1 = a.l1;
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  constexpr int kCo = kDim + 8;
+  float* cm = cb;        // [4][16]
+  float* cl = cm + 64;   // [4][16]
+  float* co = cl + 64;   // [4][16][kCo]
+  __syncthreads();
+  if (t == 0) {
+    cm[warp * 16 + g] = a.m0, cm[warp * 16 + g + 8] = a.m1;
+    cl[warp * 16 + g] = l0, cl[warp * 16 + g + 8] = l1;
+  }
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) {
+    *reinterpret_cast<float2*>(co + (warp * 16 + g) * kCo + 8 * nd + 2 * t) = make_float2(a.o[nd][0], a.o[nd][1]);
+    *reinterpret_cast<float2*>(co + (warp * 16 + g + 8) * kCo + 8 * nd + 2 * t) = make_float2(a.o[nd][2], a.o[nd][3]);
+  }
+  __syncthreads();
+  const int hh = tid >> 3, dq = 4 * (tid & 7);
+  M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 16 + hh]);
+  float wgt[4];
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    wgt[w] = M == -INFINITY ? 0.f : exp2f(cm[w * 16 + hh] - M);
+    L += wgt[w] * cl[w * 16 + hh];
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 c = *reinterpret_cast<const float4*>(co + (w * 16 + hh) * kCo + dq + 32 * j);
+      acc[j].x += wgt[w] * c.x, acc[j].y += wgt[w] * c.y, acc[j].z += wgt[w] * c.z, acc[j].w += wgt[w] * c.w;
+    }
+  }
+}
+
+// dims dq + 32j of one head's output row, scaled by f, as bf16
+__device__ __forceinline__ void store_out_row(uint16_t* orow, int dq, const float4 (&acc)[4], float f) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint2*>(orow + dq + 32 * j) =
+        make_uint2(pack_bf16x2(acc[j].x * f, acc[j].y * f), pack_bf16x2(acc[j].z * f, acc[j].w * f));
+}
+
+// TMA copies of one page (K and V of KV head h) into a ring slot; bad ids
+// are flagged and replaced by page 0
+template <int KV>
+__device__ __forceinline__ void issue_page(const SparsePaParams& p, int64_t id, int h, uint8_t* slot, uint64_t* bar) {
+  constexpr int SB = PaFmt<KV>::kSlot;
+  if (id < 0 || id >= p.num_ids) {
+    set_err(p.err, BSP_DEVERR_PAGE_ID);
+    id = 0;
+  }
+  mbar_arrive_expect_tx(bar, SB);
+  if (KV == BSP_MXFP4) {
+    const int64_t blk = id / kPagesPerSide, u = id % kPagesPerSide;
+    const uint8_t* kf = p.k_base + blk * p.id_stride + static_cast<int64_t>(h) * kMxField;
+    const uint8_t* vf = p.v_base + blk * p.id_stride + static_cast<int64_t>(h) * kMxField;
+    bulk_g2s(slot, kf + u * 1024, 1024, bar);
+    bulk_g2s(slot + 1024, kf + kMxScaleOff + u * 64, 64, bar);
+    bulk_g2s(slot + 1088, vf + u * 1024, 1024, bar);
+    bulk_g2s(slot + 2112, vf + kMxScaleOff + u * 64, 64, bar);
+  } else {
+    constexpr int PB = SB / 2;
+    bulk_g2s(slot, p.k_base + id * p.id_stride + static_cast<int64_t>(h) * PB, PB, bar);
+    bulk_g2s(slot + PB, p.v_base + id * p.id_stride + static_cast<int64_t>(h) * PB, PB, bar);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-row schedule: CTA = (row, split)
 template <int KV>
 __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
   constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
-  constexpr bool F16 = KV == BSP_FP8_E4M3;  // f16 mma with permuted tokens; else bf16
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>());
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t cta = blockIdx.x;
   const int row = static_cast<int>(cta / p.nsplit), split = static_cast<int>(cta % p.nsplit);
   const int h = row % p.hkv;
   const int64_t token = row / p.hkv;
   const int hq = p.hkv * p.group;
-  const int ctx = min(max(p.sparse_ctx[row], 0), p.k_pages * kPage);
-  const int npages = (ctx + kPage - 1) / kPage;
-  const int p0 = split * p.pages_per_split, p1 = min(p0 + p.pages_per_split, npages);
 
   if (tid == 0) {
     for (int i = 0; i < 4 * R; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the sparse table and the queries come from earlier kernels
+  pdl_trigger();
 
+  const int ctx = min(max(p.sparse_ctx[row], 0), p.k_pages * kPage);
+  const int npages = (ctx + kPage - 1) / kPage;
+  const int p0 = split * p.pages_per_split, p1 = min(p0 + p.pages_per_split, npages);
   const int nw = p1 > p0 + warp ? (p1 - p0 - warp + 3) / 4 : 0;
   const int32_t* sbt = p.sparse_bt + static_cast<int64_t>(row) * p.k_pages;
   uint8_t* wring = smem + warp * R * SB;
@@ -214,270 +512,53 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
     }
     return __shfl_sync(0xffffffffu, my_id, j & 31);
   };
-  auto issue = [&](int i, int64_t id) {
-    if (id < 0 || id >= p.num_ids) {
-      set_err(p.err, BSP_DEVERR_PAGE_ID);
-      id = 0;
-    }
-    uint8_t* slot = wring + (i % R) * SB;
-    uint64_t* bar = &wbar[i % R];
-    mbar_arrive_expect_tx(bar, SB);
-    if (KV == BSP_MXFP4) {
-      const int64_t blk = id / kPagesPerSide, u = id % kPagesPerSide;
-      const uint8_t* kf = p.k_base + blk * p.id_stride + static_cast<int64_t>(h) * kMxField;
-      const uint8_t* vf = p.v_base + blk * p.id_stride + static_cast<int64_t>(h) * kMxField;
-      bulk_g2s(slot, kf + u * 1024, 1024, bar);
-      bulk_g2s(slot + 1024, kf + kMxScaleOff + u * 64, 64, bar);
-      bulk_g2s(slot + 1088, vf + u * 1024, 1024, bar);
-      bulk_g2s(slot + 2112, vf + kMxScaleOff + u * 64, 64, bar);
-    } else {
-      constexpr int PB = SB / 2;
-      bulk_g2s(slot, p.k_base + id * p.id_stride + static_cast<int64_t>(h) * PB, PB, bar);
-      bulk_g2s(slot + PB, p.v_base + id * p.id_stride + static_cast<int64_t>(h) * PB, PB, bar);
-    }
-  };
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int32_t id = id_of(i);
-    if (lane == 0 && i < nw) issue(i, id);
+    if (lane == 0 && i < nw) issue_page<KV>(p, id, h, wring + i * SB, &wbar[i]);
   }
 
-  // Q fragments (A operand), rows = heads g and g+8 of this KV head
   uint32_t qa[8][4];
-  {
-    const int64_t qrow = (token * hq + static_cast<int64_t>(h) * p.group) * kDim;
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc) {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int head = g + 8 * half;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (F16) {
-          if (head < p.group) load_q_vals(p.q, p.q_dtype, qrow + head * kDim + 16 * kc + 4 * t, 4, v);
-          qa[kc][half] = pack_f16x2(v[0], v[1]);
-          qa[kc][2 + half] = pack_f16x2(v[2], v[3]);
-        } else {
-          if (head < p.group) {
-            load_q_vals(p.q, p.q_dtype, qrow + head * kDim + 16 * kc + 2 * t, 2, v);
-            load_q_vals(p.q, p.q_dtype, qrow + head * kDim + 16 * kc + 8 + 2 * t, 2, v + 2);
-          }
-          qa[kc][half] = pack_bf16x2(v[0], v[1]);
-          qa[kc][2 + half] = pack_bf16x2(v[2], v[3]);
-        }
-      }
-    }
-  }
+  load_q_frags<KV>(qa, p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, lane);
 
-  float o[16][4];
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
+  PaState a;
+  pa_state_init(a);
+  bool alive = true;  // false after a timed-out wait: no further waits
   for (int i = 0; i < nw; ++i) {
     const int st = i % R;
-    mbar_wait(&wbar[st], (i / R) & 1, p.err);
+    if (alive) alive = mbar_wait(&wbar[st], (i / R) & 1, p.err);
     const int pg = p0 + warp + 4 * i;
-    uint32_t kaddr, vaddr;
     if (KV == BSP_MXFP4) {
+      __syncwarp();  // every lane is done reading the previous dequantised page
       mx_page_to_bf16(wring + st * SB, wdq, lane);
       __syncwarp();
-      {
-        const int32_t id = id_of(i + R);
-        if (lane == 0 && i + R < nw) {
-          fence_proxy_async();
-          issue(i + R, id);
-        }
-      }
-      kaddr = smem_u32(wdq);
-      vaddr = kaddr + 4096;
-    } else {
-      kaddr = smem_u32(wring + st * SB);
-      vaddr = kaddr + SB / 2;
-    }
-
-    // S = Q Kt: both 8-token n-tiles interleaved, two accumulators each, so
-    // no mma waits on the one before it for more than 4 steps
-    float s[2][4];
-    {
-      float acc[2][2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) acc[nt][e][0] = acc[nt][e][1] = acc[nt][e][2] = acc[nt][e][3] = 0.f;
-      if (F16) {
-        const int rr = lane & 7;
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          uint32_t r[2][4];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const int tok = 4 * (rr >> 1) + 2 * nt + (rr & 1);
-            ldsm_x4(r[nt][0], r[nt][1], r[nt][2], r[nt][3], kaddr + (4 * q4 + (lane >> 3)) * 256 + tok * 16);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int kc = 4 * q4 + j;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              uint32_t b0, b1;
-              kv_e4m3x4_to_f16x2(r[nt][j], b0, b1);
-              mma_f16(acc[nt][j & 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int kc = 2 * q4;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            uint32_t r[4];
-            ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + (8 * nt + (lane & 7)) * 16);
-            mma_bf16(acc[nt][0], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], r[0], r[1]);
-            mma_bf16(acc[nt][1], qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], r[2], r[3]);
-          }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
-          s[nt][j] = pg * kPage + tok < ctx ? (acc[nt][0][j] + acc[nt][1][j]) * qk_scale : -INFINITY;
-        }
-    }
-
-    // online softmax (log2 domain); rows g (regs 0,1) and g+8 (regs 2,3)
-    float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-    float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    // The reference max moves only when a row's max grows by more than 2^8
-    // (kRescaleLog2): P then stays below 256, exact enough in f16/bf16 and far
-    // from overflow, and O is rescaled only on the (warp-uniform) pages where
-    // some row's max moved.  softmax = exp2(s - m) / sum is the same for any m.
-    const bool move0 = mx0 > m0 + kRescaleLog2, move1 = mx1 > m1 + kRescaleLog2;
-    const float mn0 = move0 ? mx0 : m0, mn1 = move1 ? mx1 : m1;
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    m0 = mn0, m1 = mn1;
-    float pr[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = exp2f(s[nt][0] - mn0);
-      pr[nt][1] = exp2f(s[nt][1] - mn0);
-      pr[nt][2] = exp2f(s[nt][2] - mn1);
-      pr[nt][3] = exp2f(s[nt][3] - mn1);
-    }
-    l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
-    l1 = l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
-    if (__any_sync(0xffffffffu, move0 || move1)) {
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        o[nd][0] *= al0, o[nd][1] *= al0, o[nd][2] *= al1, o[nd][3] *= al1;
-      }
-    }
-
-    // O += P V
-    uint32_t pa0, pa1, pa2, pa3;
-    if (F16) {
-      pa0 = pack_f16x2(pr[0][0], pr[0][1]);
-      pa1 = pack_f16x2(pr[0][2], pr[0][3]);
-      pa2 = pack_f16x2(pr[1][0], pr[1][1]);
-      pa3 = pack_f16x2(pr[1][2], pr[1][3]);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t r[4];
-        ldsm_x4(r[0], r[1], r[2], r[3], vaddr + (8 * (4 * q4 + (lane >> 3)) + (lane & 7)) * 16);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t b0, b1;
-          kv_e4m3x4_to_f16x2(r[j], b0, b1);
-          mma_f16(o[4 * q4 + j], pa0, pa1, pa2, pa3, b0, b1);
-        }
-      }
-    } else {
-      // bf16 P carries 8 significant bits; P = hi + lo (both bf16) keeps ~16
-      uint32_t lo0, lo1, lo2, lo3;
-      split_bf16x2(pr[0][0], pr[0][1], pa0, lo0);
-      split_bf16x2(pr[0][2], pr[0][3], pa1, lo1);
-      split_bf16x2(pr[1][0], pr[1][1], pa2, lo2);
-      split_bf16x2(pr[1][2], pr[1][3], pa3, lo3);
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        uint32_t r[4];
-        ldsm_x4(r[0], r[1], r[2], r[3],
-                vaddr + ((lane >> 3) & 1) * 2048 + (8 * (2 * q8 + (lane >> 4)) + (lane & 7)) * 16);
-        mma_bf16(o[2 * q8], pa0, pa1, pa2, pa3, r[0], r[1]);
-        mma_bf16(o[2 * q8], lo0, lo1, lo2, lo3, r[0], r[1]);
-        mma_bf16(o[2 * q8 + 1], pa0, pa1, pa2, pa3, r[2], r[3]);
-        mma_bf16(o[2 * q8 + 1], lo0, lo1, lo2, lo3, r[2], r[3]);
-      }
-    }
-    __syncwarp();
-    if (KV != BSP_MXFP4) {
       const int32_t id = id_of(i + R);
       if (lane == 0 && i + R < nw) {
         fence_proxy_async();
-        issue(i + R, id);
+        issue_page<KV>(p, id, h, wring + st * SB, &wbar[st]);
+      }
+      pa_page<KV>(a, qa, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
+    } else {
+      pa_page<KV>(a, qa, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx, qk_scale,
+                  lane);
+      __syncwarp();
+      const int32_t id = id_of(i + R);
+      if (lane == 0 && i + R < nw) {
+        fence_proxy_async();
+        issue_page<KV>(p, id, h, wring + st * SB, &wbar[st]);
       }
     }
   }
 
-  // sum l over the quad (the 4 threads of a head row)
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-  // merge the four warps in shared memory (the rings are no longer used);
-  // rows padded to 136 floats so the fragment stores hit each bank twice at most
-  constexpr int kCo = kDim + 8;
-  __syncthreads();
-  float* cm = reinterpret_cast<float*>(smem);  // [4][16]
-  float* cl = cm + 64;                         // [4][16]
-  float* co = cl + 64;                         // [4][16][kCo]
-  if (t == 0) {
-    cm[warp * 16 + g] = m0, cm[warp * 16 + g + 8] = m1;
-    cl[warp * 16 + g] = l0, cl[warp * 16 + g + 8] = l1;
-  }
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    *reinterpret_cast<float2*>(co + (warp * 16 + g) * kCo + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
-    *reinterpret_cast<float2*>(co + (warp * 16 + g + 8) * kCo + 8 * nd + 2 * t) = make_float2(o[nd][2], o[nd][3]);
-  }
-  __syncthreads();
-  // thread -> head hh, dims 4*(tid%8) + 32*j (j < 4): 128 contiguous bytes per 8 lanes
-  const int hh = tid >> 3, dq = 4 * (tid & 7);
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 16 + hh]);
-  float wgt[4], L = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    wgt[w] = M == -INFINITY ? 0.f : exp2f(cm[w * 16 + hh] - M);
-    L += wgt[w] * cl[w * 16 + hh];
-  }
+  // merge the four warps (the rings are no longer used)
+  float* cm = reinterpret_cast<float*>(smem);
+  float M, L;
   float4 acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float4 c = *reinterpret_cast<const float4*>(co + (w * 16 + hh) * kCo + dq + 32 * j);
-      acc[j].x += wgt[w] * c.x, acc[j].y += wgt[w] * c.y, acc[j].z += wgt[w] * c.z, acc[j].w += wgt[w] * c.w;
-    }
-  }
+  pa_combine(cm, a, tid, M, L, acc);
+  const int hh = tid >> 3, dq = 4 * (tid & 7);
   uint16_t* orow = static_cast<uint16_t*>(p.out) + (token * hq + static_cast<int64_t>(h) * p.group + hh) * kDim;
   if (p.nsplit == 1) {
-    if (hh < p.group) {
-      const float f = L > 0.f ? out_scale / L : 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint2*>(orow + dq + 32 * j) =
-            make_uint2(pack_bf16x2(acc[j].x * f, acc[j].y * f), pack_bf16x2(acc[j].z * f, acc[j].w * f));
-    }
+    if (hh < p.group) store_out_row(orow, dq, acc, L > 0.f ? out_scale / L : 0.f);
     return;
   }
 
@@ -536,7 +617,8 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
       Mx = fmaxf(Mx, __ldcg(wsml + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + tid) * 2));
     float Ls = 0.f;
     for (int sp = 0; sp < p.nsplit; ++sp) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(wsml + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + tid) * 2));
+      const float2 ml =
+          __ldcg(reinterpret_cast<const float2*>(wsml + ((static_cast<int64_t>(row) * p.nsplit + sp) * 16 + tid) * 2));
       const float w = (Mx == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
       sw[sp * 16 + tid] = w;
       Ls += w * ml.y;
@@ -556,43 +638,233 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
         acc[j].x += w * c.x, acc[j].y += w * c.y, acc[j].z += w * c.z, acc[j].w += w * c.w;
       }
     }
-    const float f = sinv[hh];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint2*>(orow + dq + 32 * j) =
-          make_uint2(pack_bf16x2(acc[j].x * f, acc[j].y * f), pack_bf16x2(acc[j].z * f, acc[j].w * f));
+    store_out_row(orow, dq, acc, sinv[hh]);
   }
   if (tid == 0) counters[row] = 0;  // ready for the next call
 }
 
+// ---------------------------------------------------------------------------
+// page-balanced schedule: G = gridDim.x persistent CTAs; CTA c owns the flat
+// page slots [c*W/G, (c+1)*W/G) of the [rows x k_pages] table (W = rows *
+// k_pages), slot s = row s/k_pages, page s%k_pages.  Warp w takes the range's
+// slots s0+w, s0+w+4, ...; a slot past its row's selected context is a hole
+// (no copy, no compute).
+
+// the CTA whose range holds slot s
+__device__ __forceinline__ int64_t range_of(int64_t s, int64_t W, int64_t G) { return ((s + 1) * G - 1) / W; }
+
+constexpr int32_t kHole = INT32_MIN;
+
+template <int KV>
+__global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
+    sparse_pa_stream_kernel(SparsePaParams p, float qk_scale, float out_scale) {
+  constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* cb = reinterpret_cast<float*>(smem + pa_stream_cb_offset<KV>());
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_stream_bar_offset<KV>());
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = p.k_pages;
+  const int64_t W = static_cast<int64_t>(p.num_rows) * K, G = gridDim.x, c = blockIdx.x;
+  const int64_t s0 = c * W / G, s1 = (c + 1) * W / G;
+  const int hq = p.hkv * p.group;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4 * R; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the sparse table and the queries come from earlier kernels
+  pdl_trigger();
+  if (s0 >= s1) return;
+
+  const int nw = s1 - s0 > warp ? static_cast<int>((s1 - s0 - warp + 3) / 4) : 0;
+  uint8_t* wring = smem + warp * R * SB;
+  uint64_t* wbar = bars + warp * R;
+  uint8_t* wdq = smem + 4 * R * SB + warp * DQ;
+
+  // page id of the warp's item j (slot s0 + warp + 4j), kHole past the row's context
+  auto fetch = [&](int j) -> int32_t {
+    if (j >= nw) return kHole;
+    const int64_t s = s0 + warp + 4 * static_cast<int64_t>(j);
+    const int64_t r = s / K;
+    const int pg = static_cast<int>(s - r * K);
+    const int ctx = min(max(p.sparse_ctx[r], 0), K * kPage);
+    return pg * kPage < ctx ? p.sparse_bt[s] : kHole;
+  };
+  // lane l caches the id of item 32*id_chunk + l (loaded 32 at a time)
+  int32_t my_id = fetch(lane);
+  int id_chunk = 0;
+  auto id_of = [&](int j) -> int32_t {  // warp-uniform j
+    if ((j >> 5) != id_chunk) {
+      id_chunk = j >> 5;
+      my_id = fetch(32 * id_chunk + lane);
+    }
+    return __shfl_sync(0xffffffffu, my_id, j & 31);
+  };
+  // bit (j % R): ring item j is a hole; its phase is completed by a plain
+  // arrival so that the ring's phase parity stays (j / R) & 1
+  uint32_t holes = 0;
+  auto issue = [&](int j, int32_t id) {  // all lanes; lane 0 issues
+    const int st = j % R;
+    if (id == kHole) {
+      holes |= 1u << st;
+      if (lane == 0) mbar_arrive(&wbar[st]);
+      return;
+    }
+    holes &= ~(1u << st);
+    if (lane == 0) {
+      const int64_t s = s0 + warp + 4 * static_cast<int64_t>(j);
+      issue_page<KV>(p, id, static_cast<int>((s / K) % p.hkv), wring + st * SB, &wbar[st]);
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int32_t id = id_of(j);
+    if (j < nw) issue(j, id);
+  }
+
+  const int64_t r_first = s0 / K, r_last = (s1 - 1) / K;
+  int64_t r = r_first;
+  uint32_t qa[8][4];
+  auto q_row = [&](int64_t row) -> int64_t {
+    return ((row / p.hkv) * hq + static_cast<int64_t>(row % p.hkv) * p.group) * kDim;
+  };
+  load_q_frags<KV>(qa, p.q, p.q_dtype, q_row(r), p.group, lane);
+  const int qbytes = p.group * kDim * (p.q_dtype == BSP_BF16 ? 2 : 1);
+
+  int i = 0;
+  bool alive = true;  // false after a timed-out wait: no further waits
+  for (;;) {
+    // pull the next row's queries towards L2 while this row streams
+    if (r < r_last && tid * 128 < qbytes) {
+      const char* qn = static_cast<const char*>(p.q) + q_row(r + 1) * (p.q_dtype == BSP_BF16 ? 2 : 1) + tid * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
+    }
+    const int64_t seg_end = min(s1, (r + 1) * K);
+    const int ctx = min(max(p.sparse_ctx[r], 0), K * kPage);
+    PaState a;
+    pa_state_init(a);
+    for (; i < nw && s0 + warp + 4 * static_cast<int64_t>(i) < seg_end; ++i) {
+      const int st = i % R;
+      if (alive) alive = mbar_wait(&wbar[st], (i / R) & 1, p.err);
+      const bool hole = (holes >> st) & 1;
+      const int pg = static_cast<int>(s0 + warp + 4 * static_cast<int64_t>(i) - r * K);
+      if (KV == BSP_MXFP4) {
+        __syncwarp();  // every lane is done reading the previous dequantised page
+        if (!hole) mx_page_to_bf16(wring + st * SB, wdq, lane);
+        __syncwarp();
+        const int32_t id = id_of(i + R);
+        if (i + R < nw) {
+          if (lane == 0) fence_proxy_async();
+          issue(i + R, id);
+        }
+        if (!hole) pa_page<KV>(a, qa, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
+      } else {
+        if (!hole)
+          pa_page<KV>(a, qa, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx,
+                      qk_scale, lane);
+        __syncwarp();
+        const int32_t id = id_of(i + R);
+        if (i + R < nw) {
+          if (lane == 0) fence_proxy_async();
+          issue(i + R, id);
+        }
+      }
+    }
+
+    float M, L;
+    float4 acc[4];
+    pa_combine(cb, a, tid, M, L, acc);
+    const int hh = tid >> 3, dq = 4 * (tid & 7);
+    uint16_t* orow = static_cast<uint16_t*>(p.out) + (q_row(r) + static_cast<int64_t>(hh) * kDim);
+    if (r * K >= s0 && (r + 1) * K <= s1) {
+      // the whole row is in this range
+      if (hh < p.group) store_out_row(orow, dq, acc, L > 0.f ? out_scale / L : 0.f);
+    } else {
+      // publish this range's partial of the row: unit 2c for the range's
+      // first row, 2c+1 for its last; the last range to arrive merges
+      int32_t* counters = reinterpret_cast<int32_t*>(p.ws);
+      float* wso = p.ws + ws_counter_floats(p.num_rows);
+      float* wsml = wso + 2 * G * 16 * kDim;
+      const int64_t unit = 2 * c + (r == r_first ? 0 : 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(wso + (unit * 16 + hh) * kDim + dq + 32 * j) = acc[j];
+      if ((tid & 7) == 0) *reinterpret_cast<float2*>(wsml + (unit * 16 + hh) * 2) = make_float2(M, L);
+      const int64_t cf = range_of(r * K, W, G), cl = range_of((r + 1) * K - 1, W, G);
+      const int n = static_cast<int>(cl - cf + 1);
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_last = atomicAdd(&counters[r], 1) == n - 1;
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        float* sw = cb;  // [n][16] merge weights, then [16] out_scale / L
+        float* sinv = cb + 16 * n;
+        auto unit_of = [&](int64_t cc) { return 2 * cc + ((cc * W / G) / K == r ? 0 : 1); };
+        if (tid < 16) {
+          float Mx = -INFINITY;
+          for (int k = 0; k < n; ++k) Mx = fmaxf(Mx, __ldcg(wsml + (unit_of(cf + k) * 16 + tid) * 2));
+          float Ls = 0.f;
+          for (int k = 0; k < n; ++k) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(wsml + (unit_of(cf + k) * 16 + tid) * 2));
+            const float w = (Mx == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
+            sw[k * 16 + tid] = w;
+            Ls += w * ml.y;
+          }
+          sinv[tid] = Ls > 0.f ? out_scale / Ls : 0.f;
+        }
+        __syncthreads();
+        if (hh < p.group) {
+          float4 m4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int k = 0; k < n; ++k) {
+            const float w = sw[k * 16 + hh];
+            const float* src = wso + (unit_of(cf + k) * 16 + hh) * kDim + dq;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 32 * j));
+              m4[j].x += w * v.x, m4[j].y += w * v.y, m4[j].z += w * v.z, m4[j].w += w * v.w;
+            }
+          }
+          store_out_row(orow, dq, m4, sinv[hh]);
+        }
+        if (tid == 0) counters[r] = 0;  // ready for the next call
+      }
+    }
+    if (r == r_last) break;
+    ++r;
+    load_q_frags<KV>(qa, p.q, p.q_dtype, q_row(r), p.group, lane);
+  }
+}
+
 template <int KV>
 cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
-  constexpr int bytes = pa_smem_bytes<KV>();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const bool stream = p.stream_ctas > 0;
+  const int bytes = stream ? pa_stream_smem_bytes<KV>() : pa_smem_bytes<KV>();
+  static bool configured[2] = {false, false};
+  if (!configured[stream]) {
+    cudaError_t e = stream ? cudaFuncSetAttribute(sparse_pa_stream_kernel<KV>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
+                           : cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  bytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[stream] = true;
   }
   const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * kE4m3Fold : 1.f;
   const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * kE4m3Fold : 1.f;
   const float qk_scale = p.sm_scale * kfold * kLog2e;
-  const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = bytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  if (p.cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+  cudaError_t e;
+  if (stream) {
+    e = launch_kernel(sparse_pa_stream_kernel<KV>, dim3(static_cast<unsigned>(p.stream_ctas)), dim3(128), bytes, s, 0,
+                      p, qk_scale, vfold);
+  } else {
+    const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
+    e = launch_kernel(sparse_pa_kernel<KV>, dim3(static_cast<unsigned>(ctas)), dim3(128), bytes, s, p.cluster, p,
+                      qk_scale, vfold);
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_pa_kernel<KV>, p, qk_scale, vfold);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaPeekAtLastError();
@@ -600,13 +872,23 @@ cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
 
 }  // namespace
 
-void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsplit, int32_t* pages_per_split,
-                    int32_t* cluster) {
-  // aim at one wave of about BSP_PA_CTAS_PER_SM resident CTAs per SM; split
-  // a row over up to 8 CTAs (one cluster, merged on chip) when that still
-  // covers the GPU, over more (merged through the workspace) only for very
-  // few rows
+PaPlan sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms) {
+  PaPlan plan{};
   const int64_t rows = num_rows > 0 ? num_rows : 1;
+  const int64_t W = rows * k_pages;
+  // page-balanced: every CTA streams W/G pages in one wave, when that is at
+  // least BSP_PA_STREAM_MIN_PAGES pages with the target residency
+  const int64_t G = std::min<int64_t>(static_cast<int64_t>(BSP_PA_STREAM_CTAS_PER_SM) * num_sms, kMaxStreamCtas);
+  if (BSP_PA_STREAM_MIN_PAGES > 0 && W >= G * BSP_PA_STREAM_MIN_PAGES && W < (int64_t(1) << 31)) {
+    plan.stream_ctas = static_cast<int32_t>(G);
+    plan.nsplit = 1;
+    plan.pages_per_split = k_pages;
+    return plan;
+  }
+  // per-row: aim at one wave of about BSP_PA_CTAS_PER_SM resident CTAs per
+  // SM; split a row over up to 8 CTAs (one cluster, merged on chip) when that
+  // still covers the GPU, over more (merged through the workspace) only for
+  // very few rows
   int64_t ns = (static_cast<int64_t>(BSP_PA_CTAS_PER_SM) * num_sms + rows - 1) / rows;
   const int64_t max_ns = std::min<int64_t>(64, (k_pages + 3) / 4);
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
@@ -616,15 +898,21 @@ void sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms, int32_t* nsp
   if (pps < 4) pps = 4;
   ns = (k_pages + pps - 1) / pps;
   if (ns < 1) ns = 1;
-  *nsplit = static_cast<int32_t>(ns);
-  *pages_per_split = static_cast<int32_t>(pps);
-  *cluster = (ns >= 2 && ns <= kMaxCluster) ? static_cast<int32_t>(ns) : 0;
+  plan.nsplit = static_cast<int32_t>(ns);
+  plan.pages_per_split = static_cast<int32_t>(pps);
+  plan.cluster = (ns >= 2 && ns <= kMaxCluster) ? static_cast<int32_t>(ns) : 0;
+  return plan;
 }
 
-size_t sparse_pa_ws_bytes(int32_t num_rows, int32_t nsplit) {
-  if (nsplit <= kMaxCluster) return 0;  // no split, or merged on chip in a cluster
-  return (static_cast<size_t>(ws_counter_floats(num_rows)) + static_cast<size_t>(num_rows) * nsplit * 16 * (kDim + 2)) *
-         sizeof(float);
+size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan) {
+  size_t partials;
+  if (plan.stream_ctas > 0)
+    partials = static_cast<size_t>(2) * plan.stream_ctas;  // two per range
+  else if (plan.nsplit > kMaxCluster)
+    partials = static_cast<size_t>(num_rows) * plan.nsplit;
+  else
+    return 0;  // no split, or merged on chip in a cluster
+  return (static_cast<size_t>(ws_counter_floats(num_rows)) + partials * 16 * (kDim + 2)) * sizeof(float);
 }
 
 size_t sparse_pa_counter_bytes(int32_t num_rows) { return static_cast<size_t>(ws_counter_floats(num_rows)) * 4; }

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
   const int max_len = p.max_pages * kPage;
+  pdl_wait();  // scores come from the kernel before
+  pdl_trigger();
   const int L = min(max(p.row_len[r], 0), max_len);
   const int n = (L + kPage - 1) / kPage;
   const int kk = min(p.k_pages, n);
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (r >= p.num_rows) return;
+  pdl_wait();  // scores come from the kernel before
+  pdl_trigger();
   int32_t* wbt = s_bt[threadIdx.x >> 5];
   const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
   const int max_len = p.max_pages * kPage;
@@ -252,10 +256,10 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
     uint32_t prefix = 0;
     for (int b = 31; b >= 0; --b) {
       const uint32_t cand = prefix | (1u << b);
-      unsigned c = 0;
+      unsigned c[4] = {0u, 0u, 0u, 0u};  // four chains: no long dependent add
 #pragma unroll
-      for (int i = 0; i < KPL; ++i) c += key[i] >= cand;
-      if (static_cast<int>(__reduce_add_sync(full, c)) >= need) prefix = cand;
+      for (int i = 0; i < KPL; ++i) c[i & 3] += key[i] >= cand;
+      if (static_cast<int>(__reduce_add_sync(full, (c[0] + c[1]) + (c[2] + c[3]))) >= need) prefix = cand;
     }
     tau = prefix;
     unsigned gt = 0;
@@ -297,20 +301,26 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
   }
 }
 
+// the longest rows (pages) the one-warp-per-row kernel takes; longer rows go
+// to the block radix kernel
+#ifndef BSP_TOPK_WARP_MAX
+#define BSP_TOPK_WARP_MAX 2048
+#endif
+
 template <int KPL>
 cudaError_t launch_warp(const TopkParams& p, cudaStream_t s) {
-  topk_warp_kernel<KPL><<<(p.num_rows + 3) / 4, 128, 0, s>>>(p);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(topk_warp_kernel<KPL>, dim3((p.num_rows + 3) / 4), dim3(128), 0, s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
-  if (p.max_pages <= 128) return launch_warp<4>(p, s);
-  if (p.max_pages <= 512) return launch_warp<16>(p, s);
-  if (p.max_pages <= 1024) return launch_warp<32>(p, s);
-  if (p.max_pages <= 2048) return launch_warp<64>(p, s);
+  if (p.max_pages <= 128 && BSP_TOPK_WARP_MAX >= 128) return launch_warp<4>(p, s);
+  if (p.max_pages <= 512 && BSP_TOPK_WARP_MAX >= 512) return launch_warp<16>(p, s);
+  if (p.max_pages <= 1024 && BSP_TOPK_WARP_MAX >= 1024) return launch_warp<32>(p, s);
+  if (p.max_pages <= 2048 && BSP_TOPK_WARP_MAX >= 2048) return launch_warp<64>(p, s);
   const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
   const size_t bytes = static_cast<size_t>(cand) * 4;
   static bool configured = false;
@@ -320,8 +330,8 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  topk_select_kernel<<<p.num_rows, kThreads, bytes, s>>>(p);
-  return cudaPeekAtLastError();
+  const cudaError_t e = launch_kernel(topk_select_kernel, dim3(p.num_rows), dim3(kThreads), bytes, s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace bsp

@@ -196,6 +196,53 @@ def test_attention_split_merge_paths(bsp, name):
         assert ok, (k_pages, n, worst, rl2)
 
 
+# Batches large enough for the page-balanced decode plan (rows * k_pages of
+# at least 16 pages per CTA of a 2-per-SM grid): whole rows, rows cut across
+# several CTA ranges (merged by the last range to arrive), holes past short
+# contexts, pad rows, ragged tails.
+_short = [0, 1, 17, 300, 2047, 2048, 2049, 3000]
+PAGE_BALANCED = {
+    "fp8": dict(name="pb-fp8", seed=21, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
+                hkv=1, group=16, k_pages=128, q_len=2, decode_lens=_short + list(range(2100, 4200, 88))[:24]),
+    "fp8_h2": dict(name="pb-fp8-h2", seed=22, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
+                   hkv=2, group=8, k_pages=128, q_len=1, decode_lens=_short + list(range(2500, 5000, 100))[:24]),
+    "mx": dict(name="pb-mx", seed=23, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8, idx_q_dtype=W.FP8,
+               hkv=1, group=16, k_pages=128, q_len=1, decode_lens=_short * 2 + list(range(2100, 6900, 100))[:48]),
+    "bf16": dict(name="pb-bf16", seed=24, kv_dtype=W.BF16, idx_dtype=W.BF16, q_dtype=W.BF16, idx_q_dtype=W.BF16,
+                 hkv=1, group=4, k_pages=128, q_len=4, decode_lens=[5, 2048, 2100, 2600] + [2300] * 12),
+    # few rows, the widest selection: one row is cut across ~100 ranges
+    "few_long": dict(name="pb-few-long", seed=25, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16,
+                     idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=2048, q_len=1, decode_lens=[40000, 33000, 5000]),
+}
+
+
+@pytest.mark.parametrize("name", list(PAGE_BALANCED))
+def test_attention_page_balanced(bsp, name):
+    w = W.Workload(PAGE_BALANCED[name])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = min(2 * sms, 551)
+    assert w.num_rows * w.k_pages >= 16 * G
+    # the plan's workspace: row counters, then two partials per CTA range
+    assert bsp.decode_workspace_bytes(w.num_rows, w.k_pages, w.group) == \
+        ((w.num_rows + 63) // 64 * 64 + 2 * G * 16 * 130) * 4
+    o, g = OracleSide(w), GpuSide(w)
+    ti, sb, ctx = o.topk(o.scores())
+    ref = bf16_f32(torch.from_numpy(o.attention(sb, ctx).view(np.int16)))
+    ws = bsp.decode_workspace(w.num_rows, w.k_pages, w.group)
+    for call in range(2):  # the counters are back at zero after a call
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb).cuda(),
+                                   torch.from_numpy(ctx).cuda(), w.k_pages, SM_SCALE, ws=ws, dev_err=err)
+        got = bf16_f32(out).reshape(ref.shape)
+        assert err.item() == 0
+        ok, worst, rl2 = attention_close(got, ref)
+        print(f"{name} call {call}: rows={w.num_rows} worst {worst:.3g} rel-L2 {rl2:.3g}")
+        assert ok, (call, worst, rl2)
+        assert (got[np.repeat(ctx == 0, w.group)] == 0).all()
+        counters = ws[:w.num_rows * 4].view(torch.int32)
+        assert int(counters.abs().sum().item()) == 0
+
+
 @pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx"])
 def test_pipeline_end_to_end(bsp, name):
     """GPU path and oracle path run independently from the same inputs."""
