@@ -12,9 +12,11 @@ head, top-128 pages).
 Timing: every step is bracketed by CUDA events on the launching stream; an L2
 flush (a 256 MiB memset, twice the L2) runs before each step and is not
 timed; the reported ms_per_step is the mean of the K event intervals, max over
-ranks.  The index-score and attention kernels are timed by events inside the
-step for the roofline.  SM clocks are sampled with nvidia-smi during the timed
-region.  `e2e` repeats the measurement through the public step API with the
+ranks.  Consecutive kernels of a step overlap their launch (programmatic
+dependent launch), so no event sits between them in those K steps.  The K
+steps then run once more with an event between kernels, which gives each
+kernel's duration for the roofline (an upper bound: the events serialise the
+kernels).  SM clocks are sampled with nvidia-smi during both passes.  `e2e` repeats the measurement through the public step API with the
 step's inputs copied from pinned host memory and the attention output copied
 back, inside the timed region.  `cpu_baseline` times the CPU oracle (C, OpenMP)
 on a bounded sample of the same workload; `--impl reference` reports that
@@ -314,10 +316,14 @@ def run_ours(args):
             e.record(stream)
     torch.cuda.synchronize()
 
-    def one(evs=None):
+    def one(evs=None, inner=False):
         flush.zero_()
+        if evs is not None and not inner:
+            evs[0].record(stream)
         st.run(inputs["k"], inputs["v"], inputs["idx_k"], inputs["slot"], inputs["q"], inputs["idx_q"],
-               inputs["seq_lens"], events=evs, stream=stream)
+               inputs["seq_lens"], events=evs if inner else None, stream=stream)
+        if evs is not None and not inner:
+            evs[4].record(stream)
 
     for _ in range(Wm):
         one()
@@ -329,6 +335,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.2)  # let nvidia-smi take a first sample
+    # the timed region: events at step boundaries only, so consecutive
+    # kernels keep their programmatic-launch overlap
     launches0 = bsp.launch_count()
     for i in range(K):
         one(events[i])
@@ -336,29 +344,41 @@ def run_ours(args):
     launches = bsp.launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
+    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(K)]
+    # per-kernel durations: the same steps again with an event between
+    # kernels (which serialises them, so these bound each kernel from above)
+    for i in range(K):
+        one(events[i], inner=True)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     err = int(st.dev_err.item())
-    step_ms = [events[i][0].elapsed_time(events[i][4]) for i in range(K)]
-    score_ms = [events[i][1].elapsed_time(events[i][2]) for i in range(K)]
-    attn_ms = [events[i][3].elapsed_time(events[i][4]) for i in range(K)]
+    phase_ms = {name: [events[i][a].elapsed_time(events[i][b]) for i in range(K)]
+                for name, (a, b) in {"prep": (0, 1), "index_score": (1, 2), "topk_select": (2, 3),
+                                     "sparse_pa": (3, 4)}.items()}
+    score_ms, attn_ms = phase_ms["index_score"], phase_ms["sparse_pa"]
     ms = max_over_ranks(statistics.mean(step_ms), dev)
     tokens = w.num_decode_tokens + (w.num_prefill_tokens if mixed else 0)
     value = tokens * world / (ms / 1e3)
 
-    # roofline of the dominant kernel (the index scorer streams the most bytes)
+    # rooflines of the two HBM-bound kernels; the line's `roofline` is the one
+    # with the larger share of the step
     peak, peak_kind = measured_peaks()
     score_bytes = index_algorithmic_bytes(w)
     ctx_total = int(st.sparse_ctx[:w.num_decode_rows].sum().item())
     attn_bytes = attention_algorithmic_bytes(w, ctx_total)
     score_s = statistics.mean(score_ms) / 1e3
     attn_s = statistics.mean(attn_ms) / 1e3
-    roof = {"kernel": "index_score (decode)", "bound": "hbm", "achieved": score_bytes / score_s / 1e9,
-            "peak": peak, "unit": "GB/s", "frac": score_bytes / score_s / 1e9 / peak,
-            "traffic": recorded_traffic("index_score_kernel", w.name, ["index_score.cu", "common.cuh"]),
-            "algorithmic_bytes": score_bytes, "us_per_launch": score_s * 1e6, "peak_source": peak_kind}
-    kernels = {"sparse_pa_decode+merge": {"achieved_gbs": attn_bytes / attn_s / 1e9,
-                                          "frac": attn_bytes / attn_s / 1e9 / peak,
-                                          "algorithmic_bytes": attn_bytes, "us_per_step": attn_s * 1e6}}
+    per = {"index_score": (score_bytes, score_s, "index_score_kernel", ["index_score.cu", "common.cuh"]),
+           "sparse_pa": (attn_bytes, attn_s, "sparse_pa_kernel", ["sparse_pa.cu", "common.cuh"])}
+    kernels = {}
+    for name, (nbytes, secs, kname, files) in per.items():
+        kernels[name] = {"bound": "hbm", "achieved": nbytes / secs / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": nbytes / secs / 1e9 / peak, "traffic": recorded_traffic(kname, w.name, files),
+                         "algorithmic_bytes": nbytes, "us_per_launch": secs * 1e6, "peak_source": peak_kind}
+    for name in ("prep", "topk_select"):
+        kernels[name] = {"us_per_launch": statistics.mean(phase_ms[name]) * 1e3}
+    dom = max(per, key=lambda n: per[n][1])  # the HBM kernel with the larger share of the step
+    roof = dict(kernels[dom], kernel=dom)
 
     # end to end through the public step API, inputs from pinned host memory
     e2e = None

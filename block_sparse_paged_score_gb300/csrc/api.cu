@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libbsp (declared in include/bsp.h): argument
 // validation on the host, the split plans, and the kernel launches.  Nothing
 // here allocates, synchronises or reads device memory.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -290,7 +291,11 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group) {
   (void)group;
   if (num_rows <= 0 || k_pages <= 0) return 0;
-  return sparse_pa_ws_bytes(num_rows, sparse_pa_plan(num_rows, k_pages, device_sms()));
+  // the largest of the three KV formats' plans (the query has no format)
+  size_t need = 0;
+  for (int32_t kv : {BSP_BF16, BSP_FP8_E4M3, BSP_MXFP4})
+    need = std::max(need, sparse_pa_ws_bytes(num_rows, sparse_pa_plan(kv, num_rows, k_pages, device_sms())));
+  return need;
 }
 
 static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
@@ -326,7 +331,7 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   p.out = out;
   p.err = dev_err;
   if (decode) {
-    const PaPlan plan = sparse_pa_plan(num_rows, k_pages, device_sms());
+    const PaPlan plan = sparse_pa_plan(kv->dtype, num_rows, k_pages, device_sms());
     p.nsplit = plan.nsplit;
     p.pages_per_split = plan.pages_per_split;
     p.cluster = plan.cluster;

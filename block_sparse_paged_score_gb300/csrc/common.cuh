@@ -198,14 +198,6 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-// load a float at the same shared-memory offset in CTA `rank` of the cluster
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
 
 // ---- programmatic dependent launch -----------------------------------------
 // Kernels are launched with programmatic stream serialization, so one may
@@ -216,6 +208,16 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
 // scheduled as this grid's CTAs retire.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// generic address of the same shared-memory location in CTA `rank` of the
+// cluster; plain loads through it may be scheduled freely (order them after
+// the cluster barrier that publishes the data)
+template <typename T>
+__device__ __forceinline__ const T* cluster_map(const T* local, uint32_t rank) {
+  uint64_t out;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(local)), "r"(rank));
+  return reinterpret_cast<const T*>(out);
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

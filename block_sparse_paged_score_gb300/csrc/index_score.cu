@@ -316,15 +316,23 @@ cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
   return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
+// One block per CTA while the grid is at most this many waves of resident
+// one-stage CTAs.  `work` counts every group at the batch's longest context,
+// so shorter sequences leave CTAs that only write -inf; those are the last
+// ones launched and retire at once.
+#ifndef BSP_IDX_ONE_BLOCK_WAVES
+#define BSP_IDX_ONE_BLOCK_WAVES 1.5
+#endif
+
 template <int KEY>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
-  // Small problems: one block per CTA, one stage, every CTA resident at once
-  // (the whole batch is in flight from the start).  Large ones: 2..32 blocks
-  // per CTA through a deep ring, about four waves of resident CTAs.
+  // Small problems: one block per CTA, one stage, (about) every CTA resident
+  // at once (the whole batch is in flight from the start).  Large ones: 2..32
+  // blocks per CTA through a deep ring, about four waves of resident CTAs.
   const int64_t work = static_cast<int64_t>(p.num_groups) * p.hidx * max_blocks;
   const int64_t slots1 = static_cast<int64_t>(num_sms) *
                          std::min<int64_t>(16, (227 * 1024) / smem_bytes<KEY>(1));
-  if (work <= slots1) {
+  if (work <= static_cast<int64_t>(BSP_IDX_ONE_BLOCK_WAVES * slots1)) {
     p.blocks_per_chunk = 1;
     p.stages = 1;
     return;

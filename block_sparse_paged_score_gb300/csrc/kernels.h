@@ -134,7 +134,7 @@ struct SparsePaParams {
 struct PaPlan {
   int32_t nsplit, pages_per_split, cluster, stream_ctas;
 };
-PaPlan sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms);
+PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int num_sms);
 size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan);
 // bytes of the per-row arrival counters at the start of the workspace
 size_t sparse_pa_counter_bytes(int32_t num_rows);

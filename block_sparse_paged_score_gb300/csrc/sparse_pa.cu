@@ -70,33 +70,41 @@ struct PaFmt;
 // pages in flight per warp (fp8) and the split plan's target of resident
 // CTAs per SM; compile-time so that they can be tuned by measurement
 #ifndef BSP_PA_FP8_RING
-#define BSP_PA_FP8_RING 4
+#define BSP_PA_FP8_RING 3
 #endif
+// resident CTAs per SM the per-row split plan targets (0: the kernel's
+// occupancy as the CUDA runtime reports it)
 #ifndef BSP_PA_CTAS_PER_SM
-#define BSP_PA_CTAS_PER_SM 3
+#define BSP_PA_CTAS_PER_SM 0
 #endif
 constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 // page-balanced plan: resident CTAs per SM it targets, and the fewest pages
-// per CTA (at that target) for which it is taken over the per-row plan
+// per CTA (at that target) for which it is taken over the per-row plan (0:
+// never; at 2 CTAs per SM it measured slower than the per-row plan's 3)
 #ifndef BSP_PA_STREAM_CTAS_PER_SM
 #define BSP_PA_STREAM_CTAS_PER_SM 2
 #endif
 #ifndef BSP_PA_STREAM_MIN_PAGES
-#define BSP_PA_STREAM_MIN_PAGES 16
+#define BSP_PA_STREAM_MIN_PAGES 0
 #endif
 
+// kMinCtas: resident CTAs per SM the per-row kernel is compiled for (its
+// register budget); fp8 fits four (16 warps per SM) with a 3-page ring
+#ifndef BSP_PA_FP8_MIN_CTAS
+#define BSP_PA_FP8_MIN_CTAS 4
+#endif
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
-  static constexpr int kRing = BSP_PA_FP8_RING, kSlot = 4096, kDeq = 0;
+  static constexpr int kRing = BSP_PA_FP8_RING, kSlot = 4096, kDeq = 0, kMinCtas = BSP_PA_FP8_MIN_CTAS;
 };
 template <>
 struct PaFmt<BSP_BF16> {
-  static constexpr int kRing = 2, kSlot = 8192, kDeq = 0;
+  static constexpr int kRing = 2, kSlot = 8192, kDeq = 0, kMinCtas = 2;
 };
 template <>
 struct PaFmt<BSP_MXFP4> {
   // K data 1024 | K scales 64 | V data 1024 | V scales 64
-  static constexpr int kRing = 3, kSlot = 2176, kDeq = 8192;
+  static constexpr int kRing = 3, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
 };
 
 // shared memory: the rings (and MXFP4 dequant pages) during the page loop,
@@ -111,9 +119,11 @@ __host__ __device__ constexpr int pa_bar_offset() {
              ? 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq
              : kCombineBytes;
 }
+// the row's Q fragments (4 KB) follow the ring / merge area, then the mbarriers
+constexpr int kQFragBytes = 8 * 32 * 16;
 template <int KV>
 __host__ __device__ constexpr int pa_smem_bytes() {
-  return pa_bar_offset<KV>() + 4 * PaFmt<KV>::kRing * 8;
+  return pa_bar_offset<KV>() + kQFragBytes + 4 * PaFmt<KV>::kRing * 8;
 }
 // page-balanced kernel: rings | dequant pages | merge area | mbarriers (the
 // rings stay live across the merges, so the merge area is separate)
@@ -122,8 +132,12 @@ __host__ __device__ constexpr int pa_stream_cb_offset() {
   return 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq;
 }
 template <int KV>
-__host__ __device__ constexpr int pa_stream_bar_offset() {
+__host__ __device__ constexpr int pa_stream_q_offset() {
   return pa_stream_cb_offset<KV>() + kCombineFloats * 4;
+}
+template <int KV>
+__host__ __device__ constexpr int pa_stream_bar_offset() {
+  return pa_stream_q_offset<KV>() + kQFragBytes;
 }
 template <int KV>
 __host__ __device__ constexpr int pa_stream_smem_bytes() {
@@ -203,9 +217,6 @@ __device__ __forceinline__ void mx_page_to_bf16(const uint8_t* slot, uint8_t* dq
 // the workspace starts with one int32 arrival counter per row, padded to 256 B
 __host__ __device__ constexpr int64_t ws_counter_floats(int64_t rows) { return (rows + 63) / 64 * 64; }
 
-#ifndef BSP_PA_MIN_CTAS
-#define BSP_PA_MIN_CTAS 1
-#endif
 
 
 
@@ -223,32 +234,39 @@ __device__ __forceinline__ void pa_state_init(PaState& a) {
   a.l0 = a.l1 = 0.f;
 }
 
-// Q fragments (A operand) of one row: tile rows = query heads g and g+8 of
-// the row's KV head, starting at element `qrow` of q
+// Q fragments (A operand) of one row -- tile rows = query heads g and g+8 of
+// the row's KV head, q elements from `qrow` on -- stored to shared memory at
+// qs as [kc][lane] uint4 (4 KB).  Warp w writes k-steps 2w and 2w+1; the
+// caller synchronises the CTA before the fragments are read.
 template <int KV>
-__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[8][4], const void* q, int q_dtype, int64_t qrow,
-                                             int group, int lane) {
+__device__ __forceinline__ void store_q_frags(uint32_t qs, const void* q, int q_dtype, int64_t qrow, int group,
+                                              int warp, int lane) {
   constexpr bool F16 = KV == BSP_FP8_E4M3;
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
+  for (int kk = 0; kk < 2; ++kk) {
+    const int kc = 2 * warp + kk;
+    uint32_t f[4];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int head = g + 8 * half;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
       if (F16) {
         if (head < group) load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 4 * t, 4, v);
-        qa[kc][half] = pack_f16x2(v[0], v[1]);
-        qa[kc][2 + half] = pack_f16x2(v[2], v[3]);
+        f[half] = pack_f16x2(v[0], v[1]);
+        f[2 + half] = pack_f16x2(v[2], v[3]);
       } else {
         if (head < group) {
           load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 2 * t, 2, v);
           load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 8 + 2 * t, 2, v + 2);
         }
-        qa[kc][half] = pack_bf16x2(v[0], v[1]);
-        qa[kc][2 + half] = pack_bf16x2(v[2], v[3]);
+        f[half] = pack_bf16x2(v[0], v[1]);
+        f[2 + half] = pack_bf16x2(v[2], v[3]);
       }
     }
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(qs + (kc * 32 + lane) * 16), "r"(f[0]), "r"(f[1]),
+                 "r"(f[2]), "r"(f[3])
+                 : "memory");
   }
 }
 
@@ -256,8 +274,8 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[8][4], const void* q
 // layouts for KV = fp8, bf16 layouts otherwise); tok0 = the page's first
 // token in the row, tokens >= ctx are masked.
 template <int KV>
-__device__ __forceinline__ void pa_page(PaState& a, const uint32_t (&qa)[8][4], uint32_t kaddr, uint32_t vaddr,
-                                        int tok0, int ctx, float qk_scale, int lane) {
+__device__ __forceinline__ void pa_page(PaState& a, uint32_t qs, uint32_t kaddr, uint32_t vaddr, int tok0, int ctx,
+                                        float qk_scale, int lane) {
   constexpr bool F16 = KV == BSP_FP8_E4M3;
   const int t = lane & 3;
   // S = Q Kt: both 8-token n-tiles interleaved, two accumulators each, so no
@@ -282,11 +300,12 @@ __device__ __forceinline__ void pa_page(PaState& a, const uint32_t (&qa)[8][4], 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int kc = 4 * q4 + j;
+          const uint4 qa = lds128(qs + (kc * 32 + lane) * 16);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             uint32_t b0, b1;
             kv_e4m3x4_to_f16x2(r[nt][j], b0, b1);
-            mma_f16(acc[nt][j & 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+            mma_f16(acc[nt][j & 1], qa.x, qa.y, qa.z, qa.w, b0, b1);
           }
         }
       }
@@ -294,12 +313,13 @@ __device__ __forceinline__ void pa_page(PaState& a, const uint32_t (&qa)[8][4], 
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int kc = 2 * q4;
+        const uint4 qa0 = lds128(qs + (kc * 32 + lane) * 16), qa1 = lds128(qs + ((kc + 1) * 32 + lane) * 16);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           uint32_t r[4];
           ldsm_x4(r[0], r[1], r[2], r[3], kaddr + (4 * q4 + (lane >> 3)) * 256 + (8 * nt + (lane & 7)) * 16);
-          mma_bf16(acc[nt][0], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], r[0], r[1]);
-          mma_bf16(acc[nt][1], qa[kc + 1][0], qa[kc + 1][1], qa[kc + 1][2], qa[kc + 1][3], r[2], r[3]);
+          mma_bf16(acc[nt][0], qa0.x, qa0.y, qa0.z, qa0.w, r[0], r[1]);
+          mma_bf16(acc[nt][1], qa1.x, qa1.y, qa1.z, qa1.w, r[2], r[3]);
         }
       }
     }
@@ -469,10 +489,12 @@ __device__ __forceinline__ void issue_page(const SparsePaParams& p, int64_t id, 
 // ---------------------------------------------------------------------------
 // per-row schedule: CTA = (row, split)
 template <int KV>
-__global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
+__global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
+    sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
   constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>());
+  const uint32_t qs = smem_u32(smem + pa_bar_offset<KV>());
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>() + kQFragBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t cta = blockIdx.x;
@@ -518,8 +540,8 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
     if (lane == 0 && i < nw) issue_page<KV>(p, id, h, wring + i * SB, &wbar[i]);
   }
 
-  uint32_t qa[8][4];
-  load_q_frags<KV>(qa, p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, lane);
+  store_q_frags<KV>(qs, p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, warp, lane);
+  __syncthreads();
 
   PaState a;
   pa_state_init(a);
@@ -537,9 +559,9 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
         fence_proxy_async();
         issue_page<KV>(p, id, h, wring + st * SB, &wbar[st]);
       }
-      pa_page<KV>(a, qa, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
+      pa_page<KV>(a, qs, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
     } else {
-      pa_page<KV>(a, qa, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx, qk_scale,
+      pa_page<KV>(a, qs, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx, qk_scale,
                   lane);
       __syncwarp();
       const int32_t id = id_of(i + R);
@@ -574,19 +596,38 @@ __global__ void __launch_bounds__(128, BSP_PA_MIN_CTAS) sparse_pa_kernel(SparseP
 #pragma unroll
     for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(po + hh * kDim + dq + 32 * j) = acc[j];
     cluster_sync();
-    const uint32_t rank = cluster_ctarank();
-    for (int head = static_cast<int>(rank); head < p.group; head += p.nsplit) {
-      float Mx = -INFINITY;
-      for (int sp = 0; sp < p.nsplit; ++sp) Mx = fmaxf(Mx, ld_dsmem_f32(pm + head, sp));
-      float Ls = 0.f, O = 0.f;
-      for (int sp = 0; sp < p.nsplit; ++sp) {
-        const float m = ld_dsmem_f32(pm + head, sp);
-        const float w = (Mx == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - Mx);
-        Ls += w * ld_dsmem_f32(pl + head, sp);
-        O += w * ld_dsmem_f32(po + head * kDim + tid, sp);
+    // CTA `rank` finishes heads rank, rank + nsplit, ...: 32 threads per
+    // head, 4 dims each; every peer's (m, l, O[4 dims]) is loaded at once
+    const int rank = static_cast<int>(cluster_ctarank()), ns = p.nsplit;
+    const int d = 4 * (tid & 31);
+    for (int head = rank + (tid >> 5) * ns; head < p.group; head += 4 * ns) {
+      float mv[kMaxCluster], lv[kMaxCluster];
+      float4 ov[kMaxCluster];
+#pragma unroll
+      for (int sp = 0; sp < kMaxCluster; ++sp) {
+        if (sp < ns) {
+          mv[sp] = *cluster_map(pm + head, sp);
+          lv[sp] = *cluster_map(pl + head, sp);
+          ov[sp] = *reinterpret_cast<const float4*>(cluster_map(po + head * kDim + d, sp));
+        }
       }
-      static_cast<__nv_bfloat16*>(p.out)[(token * hq + static_cast<int64_t>(h) * p.group + head) * kDim + tid] =
-          __float2bfloat16_rn(Ls > 0.f ? O * (out_scale / Ls) : 0.f);
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int sp = 0; sp < kMaxCluster; ++sp)
+        if (sp < ns) Mx = fmaxf(Mx, mv[sp]);
+      float Ls = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kMaxCluster; ++sp) {
+        if (sp < ns) {
+          const float w = (Mx == -INFINITY || mv[sp] == -INFINITY) ? 0.f : exp2f(mv[sp] - Mx);
+          Ls += w * lv[sp];
+          O.x += w * ov[sp].x, O.y += w * ov[sp].y, O.z += w * ov[sp].z, O.w += w * ov[sp].w;
+        }
+      }
+      const float f = Ls > 0.f ? out_scale / Ls : 0.f;
+      uint16_t* dst = static_cast<uint16_t*>(p.out) + (token * hq + static_cast<int64_t>(h) * p.group + head) * kDim + d;
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(O.x * f, O.y * f), pack_bf16x2(O.z * f, O.w * f));
     }
     cluster_sync();  // peers are done reading this CTA's shared memory
     return;
@@ -661,6 +702,7 @@ __global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
   constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
   extern __shared__ __align__(128) uint8_t smem[];
   float* cb = reinterpret_cast<float*>(smem + pa_stream_cb_offset<KV>());
+  const uint32_t qs = smem_u32(smem + pa_stream_q_offset<KV>());
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_stream_bar_offset<KV>());
   __shared__ int s_last;
 
@@ -727,11 +769,11 @@ __global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
 
   const int64_t r_first = s0 / K, r_last = (s1 - 1) / K;
   int64_t r = r_first;
-  uint32_t qa[8][4];
   auto q_row = [&](int64_t row) -> int64_t {
     return ((row / p.hkv) * hq + static_cast<int64_t>(row % p.hkv) * p.group) * kDim;
   };
-  load_q_frags<KV>(qa, p.q, p.q_dtype, q_row(r), p.group, lane);
+  store_q_frags<KV>(qs, p.q, p.q_dtype, q_row(r), p.group, warp, lane);
+  __syncthreads();
   const int qbytes = p.group * kDim * (p.q_dtype == BSP_BF16 ? 2 : 1);
 
   int i = 0;
@@ -760,10 +802,10 @@ __global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
           if (lane == 0) fence_proxy_async();
           issue(i + R, id);
         }
-        if (!hole) pa_page<KV>(a, qa, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
+        if (!hole) pa_page<KV>(a, qs, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
       } else {
         if (!hole)
-          pa_page<KV>(a, qa, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx,
+          pa_page<KV>(a, qs, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx,
                       qk_scale, lane);
         __syncwarp();
         const int32_t id = id_of(i + R);
@@ -836,22 +878,33 @@ __global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
     }
     if (r == r_last) break;
     ++r;
-    load_q_frags<KV>(qa, p.q, p.q_dtype, q_row(r), p.group, lane);
+    __syncthreads();  // every warp is done with the last row's fragments
+    store_q_frags<KV>(qs, p.q, p.q_dtype, q_row(r), p.group, warp, lane);
+    __syncthreads();
   }
+}
+
+// the dynamic shared-memory opt-in of a kernel (once per process)
+template <int KV>
+cudaError_t configure_kv(bool stream) {
+  static bool configured[2] = {false, false};
+  if (configured[stream]) return cudaSuccess;
+  const cudaError_t e =
+      stream ? cudaFuncSetAttribute(sparse_pa_stream_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    pa_stream_smem_bytes<KV>())
+             : cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    pa_smem_bytes<KV>());
+  if (e == cudaSuccess) configured[stream] = true;
+  return e;
 }
 
 template <int KV>
 cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
   const bool stream = p.stream_ctas > 0;
   const int bytes = stream ? pa_stream_smem_bytes<KV>() : pa_smem_bytes<KV>();
-  static bool configured[2] = {false, false};
-  if (!configured[stream]) {
-    cudaError_t e = stream ? cudaFuncSetAttribute(sparse_pa_stream_kernel<KV>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)
-                           : cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  bytes);
+  {
+    const cudaError_t e = configure_kv<KV>(stream);
     if (e != cudaSuccess) return e;
-    configured[stream] = true;
   }
   const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * kE4m3Fold : 1.f;
   const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * kE4m3Fold : 1.f;
@@ -870,9 +923,42 @@ cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
   return cudaPeekAtLastError();
 }
 
+// resident CTAs per SM of the per-row kernel for a KV format (queried once;
+// the plan only needs it approximately, so a failed query assumes 2)
+int pa_row_occupancy(int32_t kv_dtype) {
+  static int cache[3] = {0, 0, 0};
+  const int i = kv_dtype == BSP_FP8_E4M3 ? 1 : (kv_dtype == BSP_BF16 ? 0 : 2);
+  if (BSP_PA_CTAS_PER_SM > 0) return BSP_PA_CTAS_PER_SM;
+  if (!cache[i]) {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    switch (kv_dtype) {
+      case BSP_FP8_E4M3:
+        e = configure_kv<BSP_FP8_E4M3>(false);
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_FP8_E4M3>, 128,
+                                                            pa_smem_bytes<BSP_FP8_E4M3>());
+        break;
+      case BSP_BF16:
+        e = configure_kv<BSP_BF16>(false);
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_BF16>, 128,
+                                                            pa_smem_bytes<BSP_BF16>());
+        break;
+      default:
+        e = configure_kv<BSP_MXFP4>(false);
+        if (e == cudaSuccess)
+          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_MXFP4>, 128,
+                                                            pa_smem_bytes<BSP_MXFP4>());
+    }
+    cache[i] = (e == cudaSuccess && n > 0) ? n : 2;
+  }
+  return cache[i];
+}
+
 }  // namespace
 
-PaPlan sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms) {
+PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int num_sms) {
   PaPlan plan{};
   const int64_t rows = num_rows > 0 ? num_rows : 1;
   const int64_t W = rows * k_pages;
@@ -885,11 +971,12 @@ PaPlan sparse_pa_plan(int32_t num_rows, int32_t k_pages, int num_sms) {
     plan.pages_per_split = k_pages;
     return plan;
   }
-  // per-row: aim at one wave of about BSP_PA_CTAS_PER_SM resident CTAs per
-  // SM; split a row over up to 8 CTAs (one cluster, merged on chip) when that
-  // still covers the GPU, over more (merged through the workspace) only for
-  // very few rows
-  int64_t ns = (static_cast<int64_t>(BSP_PA_CTAS_PER_SM) * num_sms + rows - 1) / rows;
+  // per-row: the fewest CTAs that fill one wave of resident CTAs -- split
+  // each row over floor(resident / rows) CTAs (fewer, longer CTAs stream
+  // better than many short ones); up to 8 splits form one cluster and merge
+  // on chip, more (very few rows) merge through the workspace
+  const int64_t resident = static_cast<int64_t>(pa_row_occupancy(kv_dtype)) * num_sms;
+  int64_t ns = resident / rows;
   const int64_t max_ns = std::min<int64_t>(64, (k_pages + 3) / 4);
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   if (ns > kMaxCluster && rows * kMaxCluster >= num_sms) ns = kMaxCluster;

@@ -4,9 +4,11 @@
 // tail page is always selected"; vLLM API docs of
 // MiniMaxM3SparseAiterPAMetadataBuilder: the page-16 rebase B*16 + j).
 //
-// Rows of up to 2048 pages: one warp per row (topk_warp_kernel).  Longer
-// rows: one CTA of 512 threads per row.  Scores become order-preserving uint32
-// keys (-0 folded onto +0) kept in shared memory.  A most-significant-digit
+// Rows of up to 128 pages: one warp per row (topk_warp_kernel).  Up to 4096:
+// one CTA of 256 threads per row with the keys in registers
+// (topk_cta_kernel).  Longer rows: one CTA of 512 threads per row with the
+// keys in shared memory (topk_select_kernel).  Scores become order-preserving
+// uint32 keys (-0 folded onto +0).  A most-significant-digit
 // radix select (four 8-bit passes, shared-memory histograms, one warp scans
 // the 256 bins) finds the k'-th largest key tau and how many keys equal to
 // tau still fit.  Selection is then "key > tau, or key == tau and among the
@@ -301,11 +303,165 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
   }
 }
 
-// the longest rows (pages) the one-warp-per-row kernel takes; longer rows go
-// to the block radix kernel
+// the longest rows (pages) the one-warp-per-row kernel takes
 #ifndef BSP_TOPK_WARP_MAX
-#define BSP_TOPK_WARP_MAX 2048
+#define BSP_TOPK_WARP_MAX 128
 #endif
+
+// One CTA of 256 threads per row of up to 256*KPT pages.  Thread t owns the
+// KPT consecutive pages t*KPT.. in registers (and the ids of the one or two
+// 128-token blocks they lie in, loaded up front).  A radix select of four
+// 8-bit passes (one shared-memory histogram per pass, one warp scans its 256
+// bins) finds tau, the need-th largest key, and how many keys equal to tau
+// are taken.  One block-wide scan of the packed per-thread counts (keys >
+// tau, keys == tau) then gives every thread the output slot of its first
+// selected page: the keys > tau before it, plus the ties before it up to the
+// number taken (the lower page wins a tie).  Pages come out in ascending
+// order with no sort.
+constexpr int kCtaThreads = 256;
+
+template <int KPT>
+__global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
+  __shared__ int s_hist[4][256];
+  __shared__ int s_warp[kCtaThreads / 32];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_above;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
+  pdl_wait();  // scores come from the kernel before
+  pdl_trigger();
+  const int max_len = p.max_pages * kPage;
+  const int L = min(max(p.row_len[r], 0), max_len);
+  const int n = (L + kPage - 1) / kPage;
+  const int kk = min(p.k_pages, n);
+  int32_t* ti = p.topk_idx + static_cast<int64_t>(r) * p.k_pages;
+  int32_t* bt = p.sparse_bt + static_cast<int64_t>(r) * p.k_pages;
+  for (int m = kk + tid; m < p.k_pages; m += kCtaThreads) ti[m] = bt[m] = -1;
+  if (kk == 0) {
+    if (tid == 0) p.sparse_ctx[r] = 0;
+    return;
+  }
+  const int n_cand = p.force_tail ? n - 1 : n;
+  const int need = p.force_tail ? kk - 1 : kk;
+  const bool all = need >= n_cand, none = need == 0, radix = !all && !none;
+
+  // independent loads: this thread's block ids and scores
+  const int first = tid * KPT;
+  const int nblk = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+  const int b0 = first / kPagesPerSide, b1 = (first + KPT - 1) / kPagesPerSide;
+  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  const int32_t id0 = b0 < nblk ? p.block_table[bt_row + b0] * p.id_mul : 0;
+  const int32_t id1 = (b1 != b0 && b1 < nblk) ? p.block_table[bt_row + b1] * p.id_mul : id0;
+  const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
+  uint32_t key[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) key[j] = (radix && first + j < n_cand) ? order_key(srow[first + j]) : 0u;
+
+  uint32_t tau = 0;
+  int take_eq = 0;
+  if (radix) {
+    uint32_t prefix = 0, mask = 0;
+    int krem = need;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      __syncthreads();  // histograms zeroed; the previous pass's digit read
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (first + j < n_cand && (key[j] & mask) == prefix) atomicAdd(&s_hist[pass][(key[j] >> shift) & 255], 1);
+      __syncthreads();
+      if (warp == 0) {
+        // lane owns bins 255-8*lane .. 248-8*lane (descending); find the digit
+        // where the running count from the top first reaches krem
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = s_hist[pass][255 - 8 * lane - j];
+          sum += c[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int run = incl - sum;  // keys in higher bins
+        if (run < krem && krem <= incl) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run < krem && krem <= run + c[j]) {
+              s_digit = static_cast<uint32_t>(255 - 8 * lane - j);
+              s_above = run;
+            }
+            run += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      krem -= s_above;
+      prefix |= s_digit << shift;
+      mask |= 255u << shift;
+    }
+    tau = prefix;
+    take_eq = krem;
+  }
+
+  // (keys > tau, keys == tau) of this thread, scanned over the block in page order
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const bool valid = first + j < n_cand;
+    gt += valid && (all || (radix && key[j] > tau));
+    eq += valid && radix && key[j] == tau;
+  }
+  const int packed = (gt << 16) | eq;  // both < 2^16
+  int x = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int before = x - packed;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  int eqr = before & 0xFFFF;
+  int pos = (before >> 16) + min(eqr, take_eq);
+  bool tail_sel = false;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int pg = first + j;
+    const bool valid = pg < n_cand;
+    const bool is_eq = valid && radix && key[j] == tau;
+    const bool sel = valid && !none && (all || (radix && key[j] > tau) || (is_eq && eqr < take_eq));
+    eqr += is_eq;
+    if (sel && pos < need) {
+      ti[pos] = pg;
+      bt[pos] = (pg / kPagesPerSide == b0 ? id0 : id1) + pg % kPagesPerSide;
+      ++pos;
+    }
+    if (pg == n - 1) tail_sel = sel;
+  }
+  // the owner of page n-1 finishes the row: the forced tail entry, and the
+  // context length (the tail page, if selected, is the last entry)
+  if (first <= n - 1 && n - 1 < first + KPT) {
+    const int pg = n - 1;
+    const int tail_len = L - kPage * (n - 1);
+    if (p.force_tail) {
+      ti[kk - 1] = pg;
+      bt[kk - 1] = (pg / kPagesPerSide == b0 ? id0 : id1) + pg % kPagesPerSide;
+      p.sparse_ctx[r] = kPage * (kk - 1) + tail_len;
+    } else {
+      p.sparse_ctx[r] = kPage * (kk - 1) + (tail_sel ? tail_len : kPage);
+    }
+  }
+}
+
+template <int KPT>
+cudaError_t launch_cta(const TopkParams& p, cudaStream_t s) {
+  const cudaError_t e = launch_kernel(topk_cta_kernel<KPT>, dim3(p.num_rows), dim3(kCtaThreads), 0, s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
+}
 
 template <int KPL>
 cudaError_t launch_warp(const TopkParams& p, cudaStream_t s) {
@@ -321,6 +477,11 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.max_pages <= 512 && BSP_TOPK_WARP_MAX >= 512) return launch_warp<16>(p, s);
   if (p.max_pages <= 1024 && BSP_TOPK_WARP_MAX >= 1024) return launch_warp<32>(p, s);
   if (p.max_pages <= 2048 && BSP_TOPK_WARP_MAX >= 2048) return launch_warp<64>(p, s);
+  if (p.max_pages <= 1 * kCtaThreads) return launch_cta<1>(p, s);
+  if (p.max_pages <= 2 * kCtaThreads) return launch_cta<2>(p, s);
+  if (p.max_pages <= 4 * kCtaThreads) return launch_cta<4>(p, s);
+  if (p.max_pages <= 8 * kCtaThreads) return launch_cta<8>(p, s);
+  if (p.max_pages <= 16 * kCtaThreads) return launch_cta<16>(p, s);
   const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
   const size_t bytes = static_cast<size_t>(cand) * 4;
   static bool configured = false;

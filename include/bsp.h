@@ -267,13 +267,16 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
  *   token m < sparse_ctx[r] of row r is token m%16 of page sparse_bt[r, m/16]
  *   out      bf16 [tokens, Hkv*G, 128] = softmax(sm_scale * q K^T) V; rows
  *            with sparse_ctx 0 get zeros
- * Split-K over pages across CTAs; the last CTA of a row to finish merges the
- * row's splits (log-sum-exp).  `ws` is a device workspace of at least
- * bsp_sparse_pa_decode_workspace_bytes(); it holds per-row arrival counters
- * that must be ZERO before the first call (e.g. cudaMemset once after
- * allocation).  Every call leaves them zero again, so a workspace is zeroed
- * once, not per call.  Calls that overlap on the GPU need separate
- * workspaces.
+ * Split-K over pages: a row's pages may be split over several CTAs whose
+ * partial results are merged by log-sum-exp -- on chip when the splits form
+ * one thread-block cluster (up to 8), else through `ws`, where the last CTA
+ * of a row to finish merges the row.  `ws` is a device workspace of at least
+ * bsp_sparse_pa_decode_workspace_bytes() (enough for any KV format; 0 when
+ * no plan for these sizes needs one, and then `ws` may be NULL).  It holds
+ * per-row arrival counters that must be ZERO before the first call (e.g.
+ * cudaMemset once after allocation).  Every call leaves them zero again, so
+ * a workspace is zeroed once, not per call.  Calls that overlap on the GPU
+ * need separate workspaces.
  * ---------------------------------------------------------------------- */
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group);
 bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,

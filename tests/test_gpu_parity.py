@@ -196,12 +196,12 @@ def test_attention_split_merge_paths(bsp, name):
         assert ok, (k_pages, n, worst, rl2)
 
 
-# Batches large enough for the page-balanced decode plan (rows * k_pages of
-# at least 16 pages per CTA of a 2-per-SM grid): whole rows, rows cut across
-# several CTA ranges (merged by the last range to arrive), holes past short
-# contexts, pad rows, ragged tails.
+# Larger decode batches: 64 rows x 128 pages (clusters of 8 splits per row,
+# or, in a build with the page-balanced plan on, rows cut across CTA ranges),
+# and 3 rows x 2048 pages (64 splits per row merged through the workspace);
+# holes past short contexts, pad rows, ragged tails.
 _short = [0, 1, 17, 300, 2047, 2048, 2049, 3000]
-PAGE_BALANCED = {
+LARGE_BATCHES = {
     "fp8": dict(name="pb-fp8", seed=21, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
                 hkv=1, group=16, k_pages=128, q_len=2, decode_lens=_short + list(range(2100, 4200, 88))[:24]),
     "fp8_h2": dict(name="pb-fp8-h2", seed=22, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
@@ -216,15 +216,9 @@ PAGE_BALANCED = {
 }
 
 
-@pytest.mark.parametrize("name", list(PAGE_BALANCED))
-def test_attention_page_balanced(bsp, name):
-    w = W.Workload(PAGE_BALANCED[name])
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    G = min(2 * sms, 551)
-    assert w.num_rows * w.k_pages >= 16 * G
-    # the plan's workspace: row counters, then two partials per CTA range
-    assert bsp.decode_workspace_bytes(w.num_rows, w.k_pages, w.group) == \
-        ((w.num_rows + 63) // 64 * 64 + 2 * G * 16 * 130) * 4
+@pytest.mark.parametrize("name", list(LARGE_BATCHES))
+def test_attention_large_batches(bsp, name):
+    w = W.Workload(LARGE_BATCHES[name])
     o, g = OracleSide(w), GpuSide(w)
     ti, sb, ctx = o.topk(o.scores())
     ref = bf16_f32(torch.from_numpy(o.attention(sb, ctx).view(np.int16)))
@@ -236,11 +230,12 @@ def test_attention_page_balanced(bsp, name):
         got = bf16_f32(out).reshape(ref.shape)
         assert err.item() == 0
         ok, worst, rl2 = attention_close(got, ref)
-        print(f"{name} call {call}: rows={w.num_rows} worst {worst:.3g} rel-L2 {rl2:.3g}")
+        print(f"{name} call {call}: rows={w.num_rows} ws={ws.numel()} worst {worst:.3g} rel-L2 {rl2:.3g}")
         assert ok, (call, worst, rl2)
         assert (got[np.repeat(ctx == 0, w.group)] == 0).all()
-        counters = ws[:w.num_rows * 4].view(torch.int32)
-        assert int(counters.abs().sum().item()) == 0
+        if ws.numel() >= w.num_rows * 4:
+            counters = ws[:w.num_rows * 4].view(torch.int32)
+            assert int(counters.abs().sum().item()) == 0
 
 
 @pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx"])
