@@ -310,7 +310,7 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   if (!valid_group(group)) return BSP_ERR_UNSUPPORTED;
   if (q_dtype != BSP_BF16 && q_dtype != BSP_FP8_E4M3) return BSP_ERR_UNSUPPORTED;
   if (num_rows == 0) return BSP_OK;
-  if (!q || !sparse_bt || !sparse_ctx || !out || !al(out, 16) || !al(q, 4)) return BSP_ERR_INVALID_ARG;
+  if (!q || !sparse_bt || !sparse_ctx || !out || !al(out, 16) || !al(q, 16)) return BSP_ERR_INVALID_ARG;
   SparsePaParams p{};
   p.kv_dtype = kv->dtype;
   p.hkv = kv->num_kv_heads;
@@ -335,15 +335,17 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
     p.nsplit = plan.nsplit;
     p.pages_per_split = plan.pages_per_split;
     p.cluster = plan.cluster;
-    p.stream_ctas = plan.stream_ctas;
+    p.ring = plan.ring;
     const size_t need = sparse_pa_ws_bytes(num_rows, plan);
     if (need) {
       if (!ws || ws_bytes < need || !al(ws, 16)) return BSP_ERR_WORKSPACE;
       p.ws = static_cast<float*>(ws);
     }
   } else {
-    p.nsplit = 1;
-    p.pages_per_split = (k_pages + 3) / 4 * 4;
+    const PaPlan plan = sparse_pa_prefill_plan(kv->dtype, k_pages);
+    p.nsplit = plan.nsplit;
+    p.pages_per_split = plan.pages_per_split;
+    p.ring = plan.ring;
   }
   int launches = 0;
   st = cuda_status(launch_sparse_pa(p, reinterpret_cast<cudaStream_t>(stream), &launches));

@@ -9,7 +9,8 @@
 // Work unit: one CTA per (query group, index head, chunk of 128-token
 // blocks).  A query group is q_group consecutive tokens of one sequence (the
 // decode query length), so the index cache of a sequence is read once per
-// group.  Thread 0 streams whole index fields (16896 B fp8, 32768 B bf16,
+// group.  The chunk length is planned from the kernel's occupancy so that the
+// grid runs in whole waves of resident CTAs.  Thread 0 streams whole index fields (16896 B fp8, 32768 B bf16,
 // 8704 B MXFP4 per block and head) into a shared-memory ring with 1-D TMA
 // bulk copies completing on mbarriers; the four warps each score 32 tokens of
 // a block (two 16-token pages) on the tensor cores:
@@ -303,46 +304,67 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   }
 }
 
+// the dynamic shared-memory opt-in (once per process; per function)
 template <int KEY>
-cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
-  static bool configured = false;  // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes<KEY>(KeyFmt<KEY>::kStages));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const cudaError_t e = launch_kernel(index_score_kernel<KEY>, grid, dim3(128), smem_bytes<KEY>(p.stages), s, 0, p);
-  return e != cudaSuccess ? e : cudaPeekAtLastError();
+cudaError_t configure_key() {
+  static bool configured = false;
+  if (configured) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_bytes<KEY>(KeyFmt<KEY>::kStages));
+  if (e == cudaSuccess) configured = true;
+  return e;
 }
 
-// One block per CTA while the grid is at most this many waves of resident
-// one-stage CTAs.  `work` counts every group at the batch's longest context,
-// so shorter sequences leave CTAs that only write -inf; those are the last
-// ones launched and retire at once.
-#ifndef BSP_IDX_ONE_BLOCK_WAVES
-#define BSP_IDX_ONE_BLOCK_WAVES 1.5
-#endif
+// resident CTAs per SM with a ring of `stages` fields (queried once per depth;
+// a failed query assumes 1)
+template <int KEY>
+int occupancy_key(int stages) {
+  static int cache[KeyFmt<KEY>::kStages + 1] = {};
+  if (!cache[stages]) {
+    int n = 0;
+    cudaError_t e = configure_key<KEY>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<KEY>, 128, smem_bytes<KEY>(stages));
+    cache[stages] = (e == cudaSuccess && n > 0) ? n : 1;
+  }
+  return cache[stages];
+}
+
+// Blocks per CTA (cb) and ring depth.  Each CTA pays a fixed start (row
+// lengths, block ids, the first copy) of about kStartBlocks blocks' worth of
+// streaming; CTAs run in waves of `resident`.  The plan minimises
+// waves * (cb + kStartBlocks) over cb = 1..32 -- whole waves, without
+// splitting a sequence's blocks finer than it pays for.  The ring holds
+// min(cb, kStages) fields, so a one-block CTA needs one stage and packs more
+// CTAs per SM.  `max_blocks` counts every group at the batch's longest
+// context; CTAs past a shorter sequence only write -inf and retire at once.
+constexpr double kStartBlocks = 1.5;
 
 template <int KEY>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
-  // Small problems: one block per CTA, one stage, (about) every CTA resident
-  // at once (the whole batch is in flight from the start).  Large ones: 2..32
-  // blocks per CTA through a deep ring, about four waves of resident CTAs.
-  const int64_t work = static_cast<int64_t>(p.num_groups) * p.hidx * max_blocks;
-  const int64_t slots1 = static_cast<int64_t>(num_sms) *
-                         std::min<int64_t>(16, (227 * 1024) / smem_bytes<KEY>(1));
-  if (work <= static_cast<int64_t>(BSP_IDX_ONE_BLOCK_WAVES * slots1)) {
-    p.blocks_per_chunk = 1;
-    p.stages = 1;
-    return;
+  const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
+  double best = 0.0;
+  for (int cb = 1; cb <= 32; ++cb) {
+    const int stages = std::min(cb, KeyFmt<KEY>::kStages);
+    const int64_t resident = static_cast<int64_t>(occupancy_key<KEY>(stages)) * num_sms;
+    const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
+    const int64_t waves = (ctas + resident - 1) / resident;
+    const double cost = static_cast<double>(waves) * (cb + kStartBlocks);
+    if (cb == 1 || cost < best) {
+      best = cost;
+      p.blocks_per_chunk = cb;
+      p.stages = stages;
+    }
+    if (cb >= max_blocks) break;
   }
-  const int S = KeyFmt<KEY>::kStages;
-  const int64_t slots = static_cast<int64_t>(num_sms) * std::max<int64_t>(1, (227 * 1024) / smem_bytes<KEY>(S));
-  int64_t cb = (work + 4 * slots - 1) / (4 * slots);
-  cb = cb < 2 ? 2 : (cb > 32 ? 32 : cb);
-  p.blocks_per_chunk = static_cast<int32_t>(cb);
-  p.stages = static_cast<int32_t>(std::min<int64_t>(S, cb));
+}
+
+template <int KEY>
+cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
+  const cudaError_t c = configure_key<KEY>();
+  if (c != cudaSuccess) return c;
+  const cudaError_t e = launch_kernel(index_score_kernel<KEY>, grid, dim3(128), smem_bytes<KEY>(p.stages), s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace
@@ -356,7 +378,10 @@ cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) 
       plan_key<BSP_BF16>(p, max_blocks, num_sms);
       break;
     case BSP_FP8_E4M3:
-      plan_key<BSP_FP8_E4M3>(p, max_blocks, num_sms);  // same field and ring as the e4m3-query form
+      if (p.q_dtype == BSP_FP8_E4M3)
+        plan_key<kFp8KeysE4m3Q>(p, max_blocks, num_sms);
+      else
+        plan_key<BSP_FP8_E4M3>(p, max_blocks, num_sms);
       break;
     default:
       plan_key<BSP_MXFP4>(p, max_blocks, num_sms);

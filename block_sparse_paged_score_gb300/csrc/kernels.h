@@ -90,7 +90,7 @@ struct IndexScoreParams {
   const int32_t* row_seq;
   const int32_t* row_len;
   int32_t num_rows, num_tokens, q_group, max_pages;
-  int32_t blocks_per_chunk, num_groups, stages;
+  int32_t blocks_per_chunk, num_groups, stages;  // filled by the launcher
   float* scores;
   int32_t* err;
 };
@@ -123,18 +123,19 @@ struct SparsePaParams {
   int32_t num_rows, k_pages;
   float sm_scale;
   void* out;
-  float* ws;  // partials: page-balanced plan, or nsplit > 8 (not clustered)
+  float* ws;  // partials when nsplit > 8 (not clustered)
   int32_t nsplit, pages_per_split;
-  int32_t cluster;      // 2..8: the row's splits form a cluster and merge on chip
-  int32_t stream_ctas;  // > 0: page-balanced persistent grid of this many CTAs
+  int32_t cluster;  // 2..8: the row's splits form a cluster and merge on chip
+  int32_t ring;     // pages in flight per warp
   int32_t* err;
 };
-// decode plan shared by the launcher and the workspace query: either the
-// page-balanced grid (stream_ctas > 0) or per-row splits
+// split plan shared by the launcher and the workspace query
 struct PaPlan {
-  int32_t nsplit, pages_per_split, cluster, stream_ctas;
+  int32_t nsplit, pages_per_split, cluster, ring;
 };
 PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int num_sms);
+// prefill: one CTA per row, written directly
+PaPlan sparse_pa_prefill_plan(int32_t kv_dtype, int32_t k_pages);
 size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan);
 // bytes of the per-row arrival counters at the start of the workspace
 size_t sparse_pa_counter_bytes(int32_t num_rows);

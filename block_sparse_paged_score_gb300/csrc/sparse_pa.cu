@@ -9,37 +9,31 @@
 // of an mma tile; unused rows are zero) over tokens m < sparse_ctx[r]; token
 // m is token m%16 of page sparse_bt[r, m/16].
 //
-// A CTA is 4 warps.  Each warp streams its pages through a ring of
-// shared-memory slots with 1-D TMA bulk copies (K page + V page of its head;
-// MXFP4: the 1 KB data and 64 B scales of both sides) completing on
+// CTA = 4 warps = one (row, split); a split is a run of pages and warp w
+// takes pages w, w+4, ... of it.  Each warp streams its pages through a ring
+// of shared-memory slots with 1-D TMA bulk copies (K page + V page of its
+// head; MXFP4: the 1 KB data and 64 B scales of both sides) completing on
 // mbarriers, and keeps its own online softmax.  Per 16-token page:
 //   S  = Q Kt : 2 n-tiles (8 tokens) x 8 k-steps of mma.sync m16n8k16
 //   P  = exp2(S*scale - m)   (log2 domain, running max m and sum l per head)
 //   O += P V  : 16 n-tiles (8 dims) of mma.sync m16n8k16
-// fp8 pages are converted to f16 in registers right after ldmatrix (exact;
-// the k/v scales are folded into the softmax scale and the output scale).
-// For fp8 the 16 tokens of a page enter the mma in the order 0,1,4,5,8,9,
-// 12,13 | 2,3,6,7,... so that the S accumulator lands as the P fragment whose
-// tokens match the V rows a ldmatrix of the dim-major V page hands each
-// thread (tokens 4t..4t+3); bf16 pages use the natural order.  MXFP4 pages
-// are dequantised by the warp into a bf16 page (e2m1 * 2^(e-127) is exact in
-// bf16) and then take the bf16 path.  The 4 warps merge in shared memory
-// (log-sum-exp).
+// The Q fragments sit in shared memory (loaded once per CTA), which keeps the
+// fp8 kernel within 128 registers: four CTAs (16 warps) per SM.  fp8 pages
+// are converted to f16 in registers right after ldmatrix (exact; the k/v
+// scales are folded into the softmax scale and the output scale).  For fp8
+// the 16 tokens of a page enter the mma in the order 0,1,4,5,8,9,12,13 |
+// 2,3,6,7,... so that the S accumulator lands as the P fragment whose tokens
+// match the V rows a ldmatrix of the dim-major V page hands each thread
+// (tokens 4t..4t+3); bf16 pages use the natural order.  MXFP4 pages are
+// dequantised by the warp into a bf16 page (e2m1 * 2^(e-127) is exact in
+// bf16) and then take the bf16 path.
 //
-// Two schedules:
-//  * per-row (sparse_pa_kernel): CTA = one (row, split), warp w takes pages
-//    w, w+4, ... of the split.  One split writes the row directly; 2..8
-//    splits form a thread-block cluster and merge through distributed shared
-//    memory; more splits publish (m, l, O) to the workspace and the last CTA
-//    of the row to arrive merges them.  Prefill (one split per row) and small
-//    decode batches use it.
-//  * page-balanced (sparse_pa_stream_kernel): a persistent grid of G CTAs
-//    cuts the flat [rows x k_pages] page table into G equal contiguous
-//    ranges, so every CTA streams the same number of pages in one wave
-//    whatever the row count.  A CTA walks its range row by row; its warps
-//    keep their rings full across row boundaries.  A row that lies wholly in
-//    one range is written directly; a row cut by range ends gets one partial
-//    per range, and the last CTA to publish one merges them.
+// The 4 warps merge in shared memory (log-sum-exp).  A row with one split is
+// written directly; 2..8 splits form a thread-block cluster and merge through
+// distributed shared memory; more splits (very few rows) publish (m, l, O) to
+// the workspace and the last CTA of the row to arrive merges them.  The plan
+// splits rows only as far as one wave of resident CTAs needs, and deepens the
+// per-warp ring (a launch parameter) when the grid leaves room for it.
 #include <algorithm>
 
 #include "common.cuh"
@@ -78,15 +72,6 @@ struct PaFmt;
 #define BSP_PA_CTAS_PER_SM 0
 #endif
 constexpr int kMaxCluster = 8;  // portable thread-block cluster size
-// page-balanced plan: resident CTAs per SM it targets, and the fewest pages
-// per CTA (at that target) for which it is taken over the per-row plan (0:
-// never; at 2 CTAs per SM it measured slower than the per-row plan's 3)
-#ifndef BSP_PA_STREAM_CTAS_PER_SM
-#define BSP_PA_STREAM_CTAS_PER_SM 2
-#endif
-#ifndef BSP_PA_STREAM_MIN_PAGES
-#define BSP_PA_STREAM_MIN_PAGES 0
-#endif
 
 // kMinCtas: resident CTAs per SM the per-row kernel is compiled for (its
 // register budget); fp8 fits four (16 warps per SM) with a 3-page ring
@@ -95,16 +80,16 @@ constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 #endif
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
-  static constexpr int kRing = BSP_PA_FP8_RING, kSlot = 4096, kDeq = 0, kMinCtas = BSP_PA_FP8_MIN_CTAS;
+  static constexpr int kRing = BSP_PA_FP8_RING, kRingMax = 6, kSlot = 4096, kDeq = 0, kMinCtas = BSP_PA_FP8_MIN_CTAS;
 };
 template <>
 struct PaFmt<BSP_BF16> {
-  static constexpr int kRing = 2, kSlot = 8192, kDeq = 0, kMinCtas = 2;
+  static constexpr int kRing = 2, kRingMax = 4, kSlot = 8192, kDeq = 0, kMinCtas = 2;
 };
 template <>
 struct PaFmt<BSP_MXFP4> {
   // K data 1024 | K scales 64 | V data 1024 | V scales 64
-  static constexpr int kRing = 3, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
+  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
 };
 
 // shared memory: the rings (and MXFP4 dequant pages) during the page loop,
@@ -114,38 +99,17 @@ constexpr int kCombineFloats = 128 + 4 * 16 * (128 + 8);
 // plus this CTA's partial (m[16], l[16], O[16][128]) that cluster peers read
 constexpr int kCombineBytes = (kCombineFloats + 32 + 16 * 128) * 4;
 template <int KV>
-__host__ __device__ constexpr int pa_bar_offset() {
-  return (4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq) > kCombineBytes
-             ? 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq
+__host__ __device__ constexpr int pa_bar_offset(int ring) {
+  return (4 * ring * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq) > kCombineBytes
+             ? 4 * ring * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq
              : kCombineBytes;
 }
 // the row's Q fragments (4 KB) follow the ring / merge area, then the mbarriers
 constexpr int kQFragBytes = 8 * 32 * 16;
 template <int KV>
-__host__ __device__ constexpr int pa_smem_bytes() {
-  return pa_bar_offset<KV>() + kQFragBytes + 4 * PaFmt<KV>::kRing * 8;
+__host__ __device__ constexpr int pa_smem_bytes(int ring) {
+  return pa_bar_offset<KV>(ring) + kQFragBytes + 4 * ring * 8;
 }
-// page-balanced kernel: rings | dequant pages | merge area | mbarriers (the
-// rings stay live across the merges, so the merge area is separate)
-template <int KV>
-__host__ __device__ constexpr int pa_stream_cb_offset() {
-  return 4 * PaFmt<KV>::kRing * PaFmt<KV>::kSlot + 4 * PaFmt<KV>::kDeq;
-}
-template <int KV>
-__host__ __device__ constexpr int pa_stream_q_offset() {
-  return pa_stream_cb_offset<KV>() + kCombineFloats * 4;
-}
-template <int KV>
-__host__ __device__ constexpr int pa_stream_bar_offset() {
-  return pa_stream_q_offset<KV>() + kQFragBytes;
-}
-template <int KV>
-__host__ __device__ constexpr int pa_stream_smem_bytes() {
-  return pa_stream_bar_offset<KV>() + 4 * PaFmt<KV>::kRing * 8;
-}
-// the merge weights of a cut row ([ranges][16] + [16]) live in the merge
-// area, which bounds the page-balanced grid
-constexpr int kMaxStreamCtas = (kCombineFloats - 16) / 16;
 
 // n (2 or 4) consecutive query elements starting at element `off`
 // (8-byte or 4-byte aligned for bf16, 4- or 2-byte for e4m3)
@@ -234,32 +198,81 @@ __device__ __forceinline__ void pa_state_init(PaState& a) {
   a.l0 = a.l1 = 0.f;
 }
 
-// Q fragments (A operand) of one row -- tile rows = query heads g and g+8 of
-// the row's KV head, q elements from `qrow` on -- stored to shared memory at
-// qs as [kc][lane] uint4 (4 KB).  Warp w writes k-steps 2w and 2w+1; the
-// caller synchronises the CTA before the fragments are read.
+// Q fragments (A operand) of one row: tile rows = query heads g and g+8 of
+// the row's KV head.  Warp w builds k-steps 2w and 2w+1 and stores them to
+// shared memory at qs as [kc][lane] uint4 (4 KB); the caller synchronises the
+// CTA before they are read.  Split in two so that the global loads are in
+// flight while the warp does other work: load_q_raw issues them (raw q
+// words, zero for heads past the group), store_q_raw converts and stores.
+struct QRaw {
+  uint32_t w[2][2][2];  // [k-step][head half][word]
+};
+
 template <int KV>
-__device__ __forceinline__ void store_q_frags(uint32_t qs, const void* q, int q_dtype, int64_t qrow, int group,
-                                              int warp, int lane) {
+__device__ __forceinline__ QRaw load_q_raw(const void* q, int q_dtype, int64_t qrow, int group, int warp, int lane) {
   constexpr bool F16 = KV == BSP_FP8_E4M3;
   const int g = lane >> 2, t = lane & 3;
+  QRaw r;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const int kc = 2 * warp + kk;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int head = g + 8 * half;
+      const int64_t e = qrow + head * kDim + 16 * kc;
+      uint32_t w0 = 0, w1 = 0;
+      if (head < group) {
+        if (q_dtype == BSP_BF16) {
+          const uint16_t* b = static_cast<const uint16_t*>(q) + e;
+          if (F16) {  // elements 4t..4t+3
+            const uint2 v = *reinterpret_cast<const uint2*>(b + 4 * t);
+            w0 = v.x, w1 = v.y;
+          } else {  // elements 2t, 2t+1 and 8+2t, 9+2t
+            w0 = *reinterpret_cast<const uint32_t*>(b + 2 * t);
+            w1 = *reinterpret_cast<const uint32_t*>(b + 8 + 2 * t);
+          }
+        } else {
+          const uint8_t* b = static_cast<const uint8_t*>(q) + e;
+          if (F16) {
+            w0 = *reinterpret_cast<const uint32_t*>(b + 4 * t);
+          } else {
+            w0 = *reinterpret_cast<const uint16_t*>(b + 2 * t);
+            w1 = *reinterpret_cast<const uint16_t*>(b + 8 + 2 * t);
+          }
+        }
+      }
+      r.w[kk][half][0] = w0;
+      r.w[kk][half][1] = w1;
+    }
+  }
+  return r;
+}
+
+template <int KV>
+__device__ __forceinline__ void store_q_raw(uint32_t qs, const QRaw& r, int q_dtype, int warp, int lane) {
+  constexpr bool F16 = KV == BSP_FP8_E4M3;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
     const int kc = 2 * warp + kk;
     uint32_t f[4];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int head = g + 8 * half;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t w0 = r.w[kk][half][0], w1 = r.w[kk][half][1];
+      float v[4];
+      if (q_dtype == BSP_BF16) {
+        v[0] = bf16_bits_to_float(w0 & 0xFFFF), v[1] = bf16_bits_to_float(w0 >> 16);
+        v[2] = bf16_bits_to_float(w1 & 0xFFFF), v[3] = bf16_bits_to_float(w1 >> 16);
+      } else if (F16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = e4m3_to_float(w0 >> (8 * i));
+      } else {
+        v[0] = e4m3_to_float(w0), v[1] = e4m3_to_float(w0 >> 8);
+        v[2] = e4m3_to_float(w1), v[3] = e4m3_to_float(w1 >> 8);
+      }
       if (F16) {
-        if (head < group) load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 4 * t, 4, v);
         f[half] = pack_f16x2(v[0], v[1]);
         f[2 + half] = pack_f16x2(v[2], v[3]);
       } else {
-        if (head < group) {
-          load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 2 * t, 2, v);
-          load_q_vals(q, q_dtype, qrow + head * kDim + 16 * kc + 8 + 2 * t, 2, v + 2);
-        }
         f[half] = pack_bf16x2(v[0], v[1]);
         f[2 + half] = pack_bf16x2(v[2], v[3]);
       }
@@ -491,10 +504,11 @@ __device__ __forceinline__ void issue_page(const SparsePaParams& p, int64_t id, 
 template <int KV>
 __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
     sparse_pa_kernel(SparsePaParams p, float qk_scale, float out_scale) {
-  constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
+  constexpr int SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
+  const int R = p.ring;  // pages in flight per warp, 1..kRingMax
   extern __shared__ __align__(128) uint8_t smem[];
-  const uint32_t qs = smem_u32(smem + pa_bar_offset<KV>());
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>() + kQFragBytes);
+  const uint32_t qs = smem_u32(smem + pa_bar_offset<KV>(R));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_bar_offset<KV>(R) + kQFragBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t cta = blockIdx.x;
@@ -511,6 +525,10 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
   pdl_wait();  // the sparse table and the queries come from earlier kernels
   pdl_trigger();
 
+  // the queries' loads go out first; they land while the page ids and the
+  // first pages are fetched
+  const QRaw qraw =
+      load_q_raw<KV>(p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, warp, lane);
   const int ctx = min(max(p.sparse_ctx[row], 0), p.k_pages * kPage);
   const int npages = (ctx + kPage - 1) / kPage;
   const int p0 = split * p.pages_per_split, p1 = min(p0 + p.pages_per_split, npages);
@@ -534,21 +552,21 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
     }
     return __shfl_sync(0xffffffffu, my_id, j & 31);
   };
-#pragma unroll
   for (int i = 0; i < R; ++i) {
     const int32_t id = id_of(i);
     if (lane == 0 && i < nw) issue_page<KV>(p, id, h, wring + i * SB, &wbar[i]);
   }
 
-  store_q_frags<KV>(qs, p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, warp, lane);
+  store_q_raw<KV>(qs, qraw, p.q_dtype, warp, lane);
   __syncthreads();
 
   PaState a;
   pa_state_init(a);
   bool alive = true;  // false after a timed-out wait: no further waits
+  int st = 0;         // ring slot of page i, and the parity of its phase
+  uint32_t phase = 0;
   for (int i = 0; i < nw; ++i) {
-    const int st = i % R;
-    if (alive) alive = mbar_wait(&wbar[st], (i / R) & 1, p.err);
+    if (alive) alive = mbar_wait(&wbar[st], phase, p.err);
     const int pg = p0 + warp + 4 * i;
     if (KV == BSP_MXFP4) {
       __syncwarp();  // every lane is done reading the previous dequantised page
@@ -570,6 +588,7 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
         issue_page<KV>(p, id, h, wring + st * SB, &wbar[st]);
       }
     }
+    if (++st == R) st = 0, phase ^= 1;
   }
 
   // merge the four warps (the rings are no longer used)
@@ -684,299 +703,61 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
   if (tid == 0) counters[row] = 0;  // ready for the next call
 }
 
-// ---------------------------------------------------------------------------
-// page-balanced schedule: G = gridDim.x persistent CTAs; CTA c owns the flat
-// page slots [c*W/G, (c+1)*W/G) of the [rows x k_pages] table (W = rows *
-// k_pages), slot s = row s/k_pages, page s%k_pages.  Warp w takes the range's
-// slots s0+w, s0+w+4, ...; a slot past its row's selected context is a hole
-// (no copy, no compute).
-
-// the CTA whose range holds slot s
-__device__ __forceinline__ int64_t range_of(int64_t s, int64_t W, int64_t G) { return ((s + 1) * G - 1) / W; }
-
-constexpr int32_t kHole = INT32_MIN;
-
+// the dynamic shared-memory opt-in of a kernel: its largest ring (once per process)
 template <int KV>
-__global__ void __launch_bounds__(128, BSP_PA_STREAM_CTAS_PER_SM)
-    sparse_pa_stream_kernel(SparsePaParams p, float qk_scale, float out_scale) {
-  constexpr int R = PaFmt<KV>::kRing, SB = PaFmt<KV>::kSlot, DQ = PaFmt<KV>::kDeq;
-  extern __shared__ __align__(128) uint8_t smem[];
-  float* cb = reinterpret_cast<float*>(smem + pa_stream_cb_offset<KV>());
-  const uint32_t qs = smem_u32(smem + pa_stream_q_offset<KV>());
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pa_stream_bar_offset<KV>());
-  __shared__ int s_last;
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int K = p.k_pages;
-  const int64_t W = static_cast<int64_t>(p.num_rows) * K, G = gridDim.x, c = blockIdx.x;
-  const int64_t s0 = c * W / G, s1 = (c + 1) * W / G;
-  const int hq = p.hkv * p.group;
-
-  if (tid == 0) {
-    for (int i = 0; i < 4 * R; ++i) mbar_init(&bars[i], 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  pdl_wait();  // the sparse table and the queries come from earlier kernels
-  pdl_trigger();
-  if (s0 >= s1) return;
-
-  const int nw = s1 - s0 > warp ? static_cast<int>((s1 - s0 - warp + 3) / 4) : 0;
-  uint8_t* wring = smem + warp * R * SB;
-  uint64_t* wbar = bars + warp * R;
-  uint8_t* wdq = smem + 4 * R * SB + warp * DQ;
-
-  // page id of the warp's item j (slot s0 + warp + 4j), kHole past the row's context
-  auto fetch = [&](int j) -> int32_t {
-    if (j >= nw) return kHole;
-    const int64_t s = s0 + warp + 4 * static_cast<int64_t>(j);
-    const int64_t r = s / K;
-    const int pg = static_cast<int>(s - r * K);
-    const int ctx = min(max(p.sparse_ctx[r], 0), K * kPage);
-    return pg * kPage < ctx ? p.sparse_bt[s] : kHole;
-  };
-  // lane l caches the id of item 32*id_chunk + l (loaded 32 at a time)
-  int32_t my_id = fetch(lane);
-  int id_chunk = 0;
-  auto id_of = [&](int j) -> int32_t {  // warp-uniform j
-    if ((j >> 5) != id_chunk) {
-      id_chunk = j >> 5;
-      my_id = fetch(32 * id_chunk + lane);
-    }
-    return __shfl_sync(0xffffffffu, my_id, j & 31);
-  };
-  // bit (j % R): ring item j is a hole; its phase is completed by a plain
-  // arrival so that the ring's phase parity stays (j / R) & 1
-  uint32_t holes = 0;
-  auto issue = [&](int j, int32_t id) {  // all lanes; lane 0 issues
-    const int st = j % R;
-    if (id == kHole) {
-      holes |= 1u << st;
-      if (lane == 0) mbar_arrive(&wbar[st]);
-      return;
-    }
-    holes &= ~(1u << st);
-    if (lane == 0) {
-      const int64_t s = s0 + warp + 4 * static_cast<int64_t>(j);
-      issue_page<KV>(p, id, static_cast<int>((s / K) % p.hkv), wring + st * SB, &wbar[st]);
-    }
-  };
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    const int32_t id = id_of(j);
-    if (j < nw) issue(j, id);
-  }
-
-  const int64_t r_first = s0 / K, r_last = (s1 - 1) / K;
-  int64_t r = r_first;
-  auto q_row = [&](int64_t row) -> int64_t {
-    return ((row / p.hkv) * hq + static_cast<int64_t>(row % p.hkv) * p.group) * kDim;
-  };
-  store_q_frags<KV>(qs, p.q, p.q_dtype, q_row(r), p.group, warp, lane);
-  __syncthreads();
-  const int qbytes = p.group * kDim * (p.q_dtype == BSP_BF16 ? 2 : 1);
-
-  int i = 0;
-  bool alive = true;  // false after a timed-out wait: no further waits
-  for (;;) {
-    // pull the next row's queries towards L2 while this row streams
-    if (r < r_last && tid * 128 < qbytes) {
-      const char* qn = static_cast<const char*>(p.q) + q_row(r + 1) * (p.q_dtype == BSP_BF16 ? 2 : 1) + tid * 128;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(qn));
-    }
-    const int64_t seg_end = min(s1, (r + 1) * K);
-    const int ctx = min(max(p.sparse_ctx[r], 0), K * kPage);
-    PaState a;
-    pa_state_init(a);
-    for (; i < nw && s0 + warp + 4 * static_cast<int64_t>(i) < seg_end; ++i) {
-      const int st = i % R;
-      if (alive) alive = mbar_wait(&wbar[st], (i / R) & 1, p.err);
-      const bool hole = (holes >> st) & 1;
-      const int pg = static_cast<int>(s0 + warp + 4 * static_cast<int64_t>(i) - r * K);
-      if (KV == BSP_MXFP4) {
-        __syncwarp();  // every lane is done reading the previous dequantised page
-        if (!hole) mx_page_to_bf16(wring + st * SB, wdq, lane);
-        __syncwarp();
-        const int32_t id = id_of(i + R);
-        if (i + R < nw) {
-          if (lane == 0) fence_proxy_async();
-          issue(i + R, id);
-        }
-        if (!hole) pa_page<KV>(a, qs, smem_u32(wdq), smem_u32(wdq) + 4096, pg * kPage, ctx, qk_scale, lane);
-      } else {
-        if (!hole)
-          pa_page<KV>(a, qs, smem_u32(wring + st * SB), smem_u32(wring + st * SB) + SB / 2, pg * kPage, ctx,
-                      qk_scale, lane);
-        __syncwarp();
-        const int32_t id = id_of(i + R);
-        if (i + R < nw) {
-          if (lane == 0) fence_proxy_async();
-          issue(i + R, id);
-        }
-      }
-    }
-
-    float M, L;
-    float4 acc[4];
-    pa_combine(cb, a, tid, M, L, acc);
-    const int hh = tid >> 3, dq = 4 * (tid & 7);
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + (q_row(r) + static_cast<int64_t>(hh) * kDim);
-    if (r * K >= s0 && (r + 1) * K <= s1) {
-      // the whole row is in this range
-      if (hh < p.group) store_out_row(orow, dq, acc, L > 0.f ? out_scale / L : 0.f);
-    } else {
-      // publish this range's partial of the row: unit 2c for the range's
-      // first row, 2c+1 for its last; the last range to arrive merges
-      int32_t* counters = reinterpret_cast<int32_t*>(p.ws);
-      float* wso = p.ws + ws_counter_floats(p.num_rows);
-      float* wsml = wso + 2 * G * 16 * kDim;
-      const int64_t unit = 2 * c + (r == r_first ? 0 : 1);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(wso + (unit * 16 + hh) * kDim + dq + 32 * j) = acc[j];
-      if ((tid & 7) == 0) *reinterpret_cast<float2*>(wsml + (unit * 16 + hh) * 2) = make_float2(M, L);
-      const int64_t cf = range_of(r * K, W, G), cl = range_of((r + 1) * K - 1, W, G);
-      const int n = static_cast<int>(cl - cf + 1);
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_last = atomicAdd(&counters[r], 1) == n - 1;
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        float* sw = cb;  // [n][16] merge weights, then [16] out_scale / L
-        float* sinv = cb + 16 * n;
-        auto unit_of = [&](int64_t cc) { return 2 * cc + ((cc * W / G) / K == r ? 0 : 1); };
-        if (tid < 16) {
-          float Mx = -INFINITY;
-          for (int k = 0; k < n; ++k) Mx = fmaxf(Mx, __ldcg(wsml + (unit_of(cf + k) * 16 + tid) * 2));
-          float Ls = 0.f;
-          for (int k = 0; k < n; ++k) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(wsml + (unit_of(cf + k) * 16 + tid) * 2));
-            const float w = (Mx == -INFINITY || ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx);
-            sw[k * 16 + tid] = w;
-            Ls += w * ml.y;
-          }
-          sinv[tid] = Ls > 0.f ? out_scale / Ls : 0.f;
-        }
-        __syncthreads();
-        if (hh < p.group) {
-          float4 m4[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) m4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int k = 0; k < n; ++k) {
-            const float w = sw[k * 16 + hh];
-            const float* src = wso + (unit_of(cf + k) * 16 + hh) * kDim + dq;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 32 * j));
-              m4[j].x += w * v.x, m4[j].y += w * v.y, m4[j].z += w * v.z, m4[j].w += w * v.w;
-            }
-          }
-          store_out_row(orow, dq, m4, sinv[hh]);
-        }
-        if (tid == 0) counters[r] = 0;  // ready for the next call
-      }
-    }
-    if (r == r_last) break;
-    ++r;
-    __syncthreads();  // every warp is done with the last row's fragments
-    store_q_frags<KV>(qs, p.q, p.q_dtype, q_row(r), p.group, warp, lane);
-    __syncthreads();
-  }
-}
-
-// the dynamic shared-memory opt-in of a kernel (once per process)
-template <int KV>
-cudaError_t configure_kv(bool stream) {
-  static bool configured[2] = {false, false};
-  if (configured[stream]) return cudaSuccess;
-  const cudaError_t e =
-      stream ? cudaFuncSetAttribute(sparse_pa_stream_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    pa_stream_smem_bytes<KV>())
-             : cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    pa_smem_bytes<KV>());
-  if (e == cudaSuccess) configured[stream] = true;
+cudaError_t configure_kv() {
+  static bool configured = false;
+  if (configured) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             pa_smem_bytes<KV>(PaFmt<KV>::kRingMax));
+  if (e == cudaSuccess) configured = true;
   return e;
 }
 
 template <int KV>
 cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
-  const bool stream = p.stream_ctas > 0;
-  const int bytes = stream ? pa_stream_smem_bytes<KV>() : pa_smem_bytes<KV>();
+  if (p.ring < 1 || p.ring > PaFmt<KV>::kRingMax) return cudaErrorInvalidValue;
   {
-    const cudaError_t e = configure_kv<KV>(stream);
+    const cudaError_t e = configure_kv<KV>();
     if (e != cudaSuccess) return e;
   }
   const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * kE4m3Fold : 1.f;
   const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * kE4m3Fold : 1.f;
   const float qk_scale = p.sm_scale * kfold * kLog2e;
-  cudaError_t e;
-  if (stream) {
-    e = launch_kernel(sparse_pa_stream_kernel<KV>, dim3(static_cast<unsigned>(p.stream_ctas)), dim3(128), bytes, s, 0,
-                      p, qk_scale, vfold);
-  } else {
-    const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
-    e = launch_kernel(sparse_pa_kernel<KV>, dim3(static_cast<unsigned>(ctas)), dim3(128), bytes, s, p.cluster, p,
-                      qk_scale, vfold);
-  }
+  const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
+  const cudaError_t e = launch_kernel(sparse_pa_kernel<KV>, dim3(static_cast<unsigned>(ctas)), dim3(128),
+                                      pa_smem_bytes<KV>(p.ring), s, p.cluster, p, qk_scale, vfold);
   if (e != cudaSuccess) return e;
   ++*launches;
   return cudaPeekAtLastError();
 }
 
-// resident CTAs per SM of the per-row kernel for a KV format (queried once;
-// the plan only needs it approximately, so a failed query assumes 2)
-int pa_row_occupancy(int32_t kv_dtype) {
-  static int cache[3] = {0, 0, 0};
-  const int i = kv_dtype == BSP_FP8_E4M3 ? 1 : (kv_dtype == BSP_BF16 ? 0 : 2);
-  if (BSP_PA_CTAS_PER_SM > 0) return BSP_PA_CTAS_PER_SM;
-  if (!cache[i]) {
+// resident CTAs per SM of the per-row kernel with a ring of `ring` pages per
+// warp (queried once per format and depth; a failed query assumes 1)
+template <int KV>
+int occupancy_kv(int ring) {
+  static int cache[PaFmt<KV>::kRingMax + 1] = {};
+  if (!cache[ring]) {
     int n = 0;
-    cudaError_t e = cudaSuccess;
-    switch (kv_dtype) {
-      case BSP_FP8_E4M3:
-        e = configure_kv<BSP_FP8_E4M3>(false);
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_FP8_E4M3>, 128,
-                                                            pa_smem_bytes<BSP_FP8_E4M3>());
-        break;
-      case BSP_BF16:
-        e = configure_kv<BSP_BF16>(false);
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_BF16>, 128,
-                                                            pa_smem_bytes<BSP_BF16>());
-        break;
-      default:
-        e = configure_kv<BSP_MXFP4>(false);
-        if (e == cudaSuccess)
-          e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<BSP_MXFP4>, 128,
-                                                            pa_smem_bytes<BSP_MXFP4>());
-    }
-    cache[i] = (e == cudaSuccess && n > 0) ? n : 2;
+    cudaError_t e = configure_kv<KV>();
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<KV>, 128, pa_smem_bytes<KV>(ring));
+    cache[ring] = (e == cudaSuccess && n > 0) ? n : 1;
   }
-  return cache[i];
+  return cache[ring];
 }
 
-}  // namespace
-
-PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int num_sms) {
+template <int KV>
+PaPlan plan_kv(int32_t num_rows, int32_t k_pages, int num_sms) {
   PaPlan plan{};
   const int64_t rows = num_rows > 0 ? num_rows : 1;
-  const int64_t W = rows * k_pages;
-  // page-balanced: every CTA streams W/G pages in one wave, when that is at
-  // least BSP_PA_STREAM_MIN_PAGES pages with the target residency
-  const int64_t G = std::min<int64_t>(static_cast<int64_t>(BSP_PA_STREAM_CTAS_PER_SM) * num_sms, kMaxStreamCtas);
-  if (BSP_PA_STREAM_MIN_PAGES > 0 && W >= G * BSP_PA_STREAM_MIN_PAGES && W < (int64_t(1) << 31)) {
-    plan.stream_ctas = static_cast<int32_t>(G);
-    plan.nsplit = 1;
-    plan.pages_per_split = k_pages;
-    return plan;
-  }
-  // per-row: the fewest CTAs that fill one wave of resident CTAs -- split
-  // each row over floor(resident / rows) CTAs (fewer, longer CTAs stream
-  // better than many short ones); up to 8 splits form one cluster and merge
-  // on chip, more (very few rows) merge through the workspace
-  const int64_t resident = static_cast<int64_t>(pa_row_occupancy(kv_dtype)) * num_sms;
-  int64_t ns = resident / rows;
+  // split each row over floor(resident / rows) CTAs: the fewest CTAs that
+  // fill one wave (fewer, longer CTAs stream better than many short ones);
+  // up to 8 splits form one cluster and merge on chip, more (very few rows)
+  // merge through the workspace
+  const int base_ring = PaFmt<KV>::kRing;
+  const int64_t per_sm = BSP_PA_CTAS_PER_SM > 0 ? BSP_PA_CTAS_PER_SM : occupancy_kv<KV>(base_ring);
+  int64_t ns = per_sm * num_sms / rows;
   const int64_t max_ns = std::min<int64_t>(64, (k_pages + 3) / 4);
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
   if (ns > kMaxCluster && rows * kMaxCluster >= num_sms) ns = kMaxCluster;
@@ -988,17 +769,42 @@ PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int n
   plan.nsplit = static_cast<int32_t>(ns);
   plan.pages_per_split = static_cast<int32_t>(pps);
   plan.cluster = (ns >= 2 && ns <= kMaxCluster) ? static_cast<int32_t>(ns) : 0;
+  // deepen the ring while the grid still fits in one wave: a warp's pages
+  // (pps / 4) all in flight at once when there is room
+  const int64_t ctas = rows * ns, per_warp = (pps + 3) / 4;
+  int ring = base_ring;
+  while (ring < PaFmt<KV>::kRingMax && ring < per_warp &&
+         static_cast<int64_t>(occupancy_kv<KV>(ring + 1)) * num_sms >= ctas)
+    ++ring;
+  plan.ring = ring;
+  return plan;
+}
+
+}  // namespace
+
+PaPlan sparse_pa_plan(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, int num_sms) {
+  switch (kv_dtype) {
+    case BSP_FP8_E4M3:
+      return plan_kv<BSP_FP8_E4M3>(num_rows, k_pages, num_sms);
+    case BSP_BF16:
+      return plan_kv<BSP_BF16>(num_rows, k_pages, num_sms);
+    default:
+      return plan_kv<BSP_MXFP4>(num_rows, k_pages, num_sms);
+  }
+}
+
+PaPlan sparse_pa_prefill_plan(int32_t kv_dtype, int32_t k_pages) {
+  PaPlan plan{};
+  plan.nsplit = 1;
+  plan.pages_per_split = (k_pages + 3) / 4 * 4;
+  plan.ring = kv_dtype == BSP_FP8_E4M3 ? PaFmt<BSP_FP8_E4M3>::kRing
+                                       : (kv_dtype == BSP_BF16 ? PaFmt<BSP_BF16>::kRing : PaFmt<BSP_MXFP4>::kRing);
   return plan;
 }
 
 size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan) {
-  size_t partials;
-  if (plan.stream_ctas > 0)
-    partials = static_cast<size_t>(2) * plan.stream_ctas;  // two per range
-  else if (plan.nsplit > kMaxCluster)
-    partials = static_cast<size_t>(num_rows) * plan.nsplit;
-  else
-    return 0;  // no split, or merged on chip in a cluster
+  if (plan.nsplit <= kMaxCluster) return 0;  // no split, or merged on chip in a cluster
+  const size_t partials = static_cast<size_t>(num_rows) * plan.nsplit;
   return (static_cast<size_t>(ws_counter_floats(num_rows)) + partials * 16 * (kDim + 2)) * sizeof(float);
 }
 

@@ -4,7 +4,7 @@
 // tail page is always selected"; vLLM API docs of
 // MiniMaxM3SparseAiterPAMetadataBuilder: the page-16 rebase B*16 + j).
 //
-// Rows of up to 128 pages: one warp per row (topk_warp_kernel).  Up to 4096:
+// Rows of up to 128 pages: one warp per row (topk_warp_kernel).  Up to 8192:
 // one CTA of 256 threads per row with the keys in registers
 // (topk_cta_kernel).  Longer rows: one CTA of 512 threads per row with the
 // keys in shared memory (topk_select_kernel).  Scores become order-preserving
@@ -345,13 +345,16 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   const int need = p.force_tail ? kk - 1 : kk;
   const bool all = need >= n_cand, none = need == 0, radix = !all && !none;
 
-  // independent loads: this thread's block ids and scores
+  // independent loads: the ids of the blocks this thread's pages lie in
+  // (pages first.. first+KPT-1 span NB blocks from b0) and its scores
+  constexpr int NB = KPT >= kPagesPerSide ? KPT / kPagesPerSide : 1;
   const int first = tid * KPT;
   const int nblk = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
-  const int b0 = first / kPagesPerSide, b1 = (first + KPT - 1) / kPagesPerSide;
+  const int b0 = first / kPagesPerSide;
   const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
-  const int32_t id0 = b0 < nblk ? p.block_table[bt_row + b0] * p.id_mul : 0;
-  const int32_t id1 = (b1 != b0 && b1 < nblk) ? p.block_table[bt_row + b1] * p.id_mul : id0;
+  int32_t ids[NB];
+#pragma unroll
+  for (int k = 0; k < NB; ++k) ids[k] = b0 + k < nblk ? p.block_table[bt_row + b0 + k] * p.id_mul : 0;
   const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
   uint32_t key[KPT];
 #pragma unroll
@@ -437,7 +440,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
     eqr += is_eq;
     if (sel && pos < need) {
       ti[pos] = pg;
-      bt[pos] = (pg / kPagesPerSide == b0 ? id0 : id1) + pg % kPagesPerSide;
+      bt[pos] = ids[KPT >= kPagesPerSide ? j / kPagesPerSide : 0] + pg % kPagesPerSide;  // first % 8 == 0 there
       ++pos;
     }
     if (pg == n - 1) tail_sel = sel;
@@ -449,7 +452,11 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
     const int tail_len = L - kPage * (n - 1);
     if (p.force_tail) {
       ti[kk - 1] = pg;
-      bt[kk - 1] = (pg / kPagesPerSide == b0 ? id0 : id1) + pg % kPagesPerSide;
+      int32_t id = ids[0];
+#pragma unroll
+      for (int k = 1; k < NB; ++k)
+        if (pg / kPagesPerSide - b0 == k) id = ids[k];
+      bt[kk - 1] = id + pg % kPagesPerSide;
       p.sparse_ctx[r] = kPage * (kk - 1) + tail_len;
     } else {
       p.sparse_ctx[r] = kPage * (kk - 1) + (tail_sel ? tail_len : kPage);
@@ -482,6 +489,7 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.max_pages <= 4 * kCtaThreads) return launch_cta<4>(p, s);
   if (p.max_pages <= 8 * kCtaThreads) return launch_cta<8>(p, s);
   if (p.max_pages <= 16 * kCtaThreads) return launch_cta<16>(p, s);
+  if (p.max_pages <= 32 * kCtaThreads) return launch_cta<32>(p, s);
   const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
   const size_t bytes = static_cast<size_t>(cand) * 4;
   static bool configured = false;

@@ -7,7 +7,7 @@ e4m3 where the workload attends or scores in e4m3, row lengths, index
 scores, top-k with the emitted sparse table, split-K attention and merge --
 on one stream, without host synchronisation.
 
-``run_from_host`` is the end-to-end form a serving loop uses: the step's
+``HostDecodeStep`` is the end-to-end form a serving loop uses: the step's
 inputs arrive in pinned host memory, are copied to the device, the step runs,
 and the attention output is copied back.
 """
@@ -62,17 +62,31 @@ class DecodeStep:
 
 
 class HostDecodeStep:
-    """End-to-end step: pinned host inputs -> device -> step -> host output."""
+    """End-to-end step: pinned host inputs -> device -> step -> host output.
+
+    The step's inputs sit back to back (256-byte aligned) in one pinned host
+    buffer, so a step makes one host-to-device copy of all of them and one
+    device-to-host copy of the attention output."""
 
     def __init__(self, step, host_inputs, device="cuda"):
         self.step = step
-        self.host = {k: v.pin_memory() for k, v in host_inputs.items()}
-        self.dev = {k: torch.empty_like(v, device=device) for k, v in self.host.items()}
+        offs, total = {}, 0
+        for k, v in host_inputs.items():
+            offs[k] = total
+            total += (v.numel() * v.element_size() + 255) // 256 * 256
+        self.nbytes = total
+        self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
+        self.dev = {}
+        for k, v in host_inputs.items():
+            n = v.numel() * v.element_size()
+            self.host_buf[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
+            self.dev[k] = self.dev_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
         self.out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
 
     @property
     def h2d_bytes(self):
-        return sum(v.numel() * v.element_size() for v in self.host.values())
+        return self.nbytes
 
     @property
     def d2h_bytes(self):
@@ -81,8 +95,7 @@ class HostDecodeStep:
     def run(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s):
-            for k, v in self.host.items():
-                self.dev[k].copy_(v, non_blocking=True)
+            self.dev_buf.copy_(self.host_buf, non_blocking=True)
             d = self.dev
             self.step.run(d["k"], d["v"], d["idx_k"], d["slot"], d["q"], d["idx_q"], d["seq_lens"], stream=s)
             self.out_host.copy_(self.step.out, non_blocking=True)

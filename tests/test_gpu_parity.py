@@ -126,13 +126,15 @@ def test_topk_bit_exact_on_oracle_scores(bsp, name):
     assert np.array_equal(gctx.cpu().numpy(), ctx)
 
 
-@pytest.mark.parametrize("max_pages", [100, 700, 2048, 3000])
+@pytest.mark.parametrize("max_pages", [100, 256, 700, 2048, 3000, 8000, 9000])
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
 def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
-    """Both selectors: one warp per row up to 2048 pages, one CTA per row beyond."""
+    """All three selectors: one warp per row up to 128 pages, one CTA with
+    the keys in registers up to 8192, one CTA with the keys in shared memory
+    beyond."""
     rng = np.random.default_rng(3)
-    rows = 300
+    rows = 300 if max_pages <= 4096 else 60
     sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
     sc[::5] = rng.standard_normal((len(sc[::5]), max_pages)).astype(np.float32)
     sc[7, ::3] = -0.0
@@ -196,10 +198,9 @@ def test_attention_split_merge_paths(bsp, name):
         assert ok, (k_pages, n, worst, rl2)
 
 
-# Larger decode batches: 64 rows x 128 pages (clusters of 8 splits per row,
-# or, in a build with the page-balanced plan on, rows cut across CTA ranges),
+# Larger decode batches: 64 rows x 128 pages (split over clusters of CTAs),
 # and 3 rows x 2048 pages (64 splits per row merged through the workspace);
-# holes past short contexts, pad rows, ragged tails.
+# short contexts, pad rows, ragged tails, deeper per-warp rings.
 _short = [0, 1, 17, 300, 2047, 2048, 2049, 3000]
 LARGE_BATCHES = {
     "fp8": dict(name="pb-fp8", seed=21, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
