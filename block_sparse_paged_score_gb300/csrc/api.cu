@@ -369,9 +369,12 @@ bsp_status bsp_sparse_pa_prefill(const bsp_kv_cache* kv, const void* q, int32_t 
 }
 
 bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* events, bsp_stream_t stream) {
-  if (!a || !a->kv || !a->idx) return BSP_ERR_INVALID_ARG;
-  const int32_t hkv = a->kv->num_kv_heads, hidx = a->idx->num_heads;
-  if (hidx != hkv) return BSP_ERR_UNSUPPORTED;  // rows are shared by the scorer and the attention
+  if (!a || !a->kv) return BSP_ERR_INVALID_ARG;
+  const bool reuse = (a->flags & BSP_REUSE_SELECTION) != 0;
+  if (!reuse && !a->idx) return BSP_ERR_INVALID_ARG;
+  const int32_t hkv = a->kv->num_kv_heads;
+  const int32_t hidx = reuse ? 0 : a->idx->num_heads;
+  if (!reuse && hidx != hkv) return BSP_ERR_UNSUPPORTED;  // rows are shared by the scorer and the attention
   if (a->num_seqs < 0 || a->q_len < 1 || a->q_len > 8) return BSP_ERR_INVALID_ARG;
   const int32_t tokens = a->num_seqs * a->q_len;
   const int32_t rows = tokens * hkv;
@@ -379,17 +382,19 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   auto mark = [&](int i) {
     if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s);
   };
-  mark(0);
-  // write + e4m3 casts + row lengths: one launch
   bsp_status st = check_kv(a->kv);
   if (st != BSP_OK) return st;
-  if ((st = check_idx(a->idx)) != BSP_OK) return st;
+  if (!reuse && (st = check_idx(a->idx)) != BSP_OK) return st;
   if (a->num_new_tokens < 0 || a->num_q_heads < 1) return BSP_ERR_INVALID_ARG;
-  if (a->num_new_tokens && (!a->k_new || !a->v_new || !a->idx_k_new || !a->slot || !al(a->k_new, 16) ||
-                            !al(a->v_new, 16) || !al(a->idx_k_new, 16) || !al(a->slot, 8)))
+  if (a->num_new_tokens && (!a->k_new || !a->v_new || !a->slot || !al(a->k_new, 16) || !al(a->v_new, 16) ||
+                            !al(a->slot, 8) || (!reuse && (!a->idx_k_new || !al(a->idx_k_new, 16)))))
     return BSP_ERR_INVALID_ARG;
-  if (!a->q || !a->idx_q || !al(a->q, 16) || !al(a->idx_q, 16) || !a->seq_lens || !a->row_seq || !a->row_len)
+  if (!a->q || !al(a->q, 16)) return BSP_ERR_INVALID_ARG;
+  if (reuse ? (!a->sparse_bt || !a->sparse_ctx)
+            : (!a->idx_q || !al(a->idx_q, 16) || !a->seq_lens || !a->row_seq || !a->row_len))
     return BSP_ERR_INVALID_ARG;
+  mark(0);
+  // write + e4m3 casts + row lengths: one launch
   const void* q = a->q;
   const void* iq = a->idx_q;
   DecodePrepParams pp{};
@@ -402,47 +407,52 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   w.num_blocks = a->kv->num_blocks;
   w.k_scale = a->kv->k_scale;
   w.v_scale = a->kv->v_scale;
-  w.idx_dtype = a->idx->dtype;
-  w.hidx = hidx;
-  w.idx_base = static_cast<uint8_t*>(a->idx->base);
-  w.idx_block_stride = a->idx->block_stride_bytes;
-  w.idx_num_blocks = a->idx->num_blocks;
+  w.hidx = hidx;  // 0: no index-key write
+  if (!reuse) {
+    w.idx_dtype = a->idx->dtype;
+    w.idx_base = static_cast<uint8_t*>(a->idx->base);
+    w.idx_block_stride = a->idx->block_stride_bytes;
+    w.idx_num_blocks = a->idx->num_blocks;
+    w.idx_k = static_cast<const uint16_t*>(a->idx_k_new);
+  }
   w.k = static_cast<const uint16_t*>(a->k_new);
   w.v = static_cast<const uint16_t*>(a->v_new);
-  w.idx_k = static_cast<const uint16_t*>(a->idx_k_new);
   w.slot = a->slot;
   w.num_tokens = a->num_new_tokens;
   w.err = a->dev_err;
   if (a->q_dtype == BSP_FP8_E4M3) {
-    if (!a->q_cast || !al(a->q_cast, 8)) return BSP_ERR_INVALID_ARG;
+    if (!a->q_cast || !al(a->q_cast, 16)) return BSP_ERR_INVALID_ARG;
     pp.cast_src[0] = static_cast<const uint16_t*>(a->q);
     pp.cast_dst[0] = static_cast<uint8_t*>(a->q_cast);
     pp.cast_n[0] = static_cast<int64_t>(tokens) * a->num_q_heads * kDim;
     q = a->q_cast;
   }
-  if (a->idx_q_dtype == BSP_FP8_E4M3) {
-    if (!a->idx_q_cast || !al(a->idx_q_cast, 8)) return BSP_ERR_INVALID_ARG;
+  if (!reuse && a->idx_q_dtype == BSP_FP8_E4M3) {
+    if (!a->idx_q_cast || !al(a->idx_q_cast, 16)) return BSP_ERR_INVALID_ARG;
     pp.cast_src[1] = static_cast<const uint16_t*>(a->idx_q);
     pp.cast_dst[1] = static_cast<uint8_t*>(a->idx_q_cast);
     pp.cast_n[1] = static_cast<int64_t>(tokens) * hidx * kDim;
     iq = a->idx_q_cast;
   }
-  pp.seq_lens = a->seq_lens;
-  pp.num_seqs = a->num_seqs;
-  pp.q_len = a->q_len;
-  pp.heads = hkv;
-  pp.row_seq = a->row_seq;
-  pp.row_len = a->row_len;
+  if (!reuse) {  // the selection's rows; nothing to compute when it is reused
+    pp.seq_lens = a->seq_lens;
+    pp.num_seqs = a->num_seqs;
+    pp.q_len = a->q_len;
+    pp.heads = hkv;
+    pp.row_seq = a->row_seq;
+    pp.row_len = a->row_len;
+  }
   if ((st = cuda_status(launch_decode_prep(pp, s))) != BSP_OK) return st;
   ++g_launches;
   mark(1);
-  if ((st = bsp_index_score(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
+  if (!reuse &&
+      (st = bsp_index_score(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
                             a->q_len, a->max_pages, a->scores, a->dev_err, stream)) != BSP_OK)
     return st;
   mark(2);
-  if ((st = bsp_topk_select(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
-                            a->kv->dtype, a->k_pages, a->flags, a->topk_idx, a->sparse_bt, a->sparse_ctx, stream)) !=
-      BSP_OK)
+  if (!reuse && (st = bsp_topk_select(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table,
+                                      a->bt_stride, a->kv->dtype, a->k_pages, a->flags & BSP_FORCE_TAIL, a->topk_idx,
+                                      a->sparse_bt, a->sparse_ctx, stream)) != BSP_OK)
     return st;
   mark(3);
   if ((st = bsp_sparse_pa_decode(a->kv, q, a->q_dtype, a->num_q_heads, a->sparse_bt, a->sparse_ctx, rows, a->k_pages,

@@ -9,11 +9,12 @@
 // Work unit: one CTA per (query group, index head, chunk of 128-token
 // blocks).  A query group is q_group consecutive tokens of one sequence (the
 // decode query length), so the index cache of a sequence is read once per
-// group.  The chunk length is planned from the kernel's occupancy so that the
-// grid runs in whole waves of resident CTAs.  Thread 0 streams whole index fields (16896 B fp8, 32768 B bf16,
-// 8704 B MXFP4 per block and head) into a shared-memory ring with 1-D TMA
-// bulk copies completing on mbarriers; the four warps each score 32 tokens of
-// a block (two 16-token pages) on the tensor cores:
+// group.  The chunk length is planned from the kernel's occupancy so that
+// the grid runs in whole waves of resident CTAs.  Thread 0 streams whole
+// index fields (16896 B fp8, 32768 B bf16, 8704 B MXFP4 per block and head)
+// into a shared-memory ring with 1-D TMA bulk copies completing on
+// mbarriers; the four warps each score 32 tokens of a block (two 16-token
+// pages) on the tensor cores:
 //   A = 16 keys x 16 dims (fp8 -> f16 exactly, e2m1 -> f16 exactly, or bf16),
 //   B = 16 dims x 8 query rows (the group's rows; unused columns are zero),
 //   C = fp32.
@@ -21,9 +22,9 @@
 // f32) straight from the cached bytes.  The dims of each mma are a
 // permutation of the real dims chosen so that every thread reads 16-byte (or
 // 4-byte) runs of a key row; A and B use the same permutation, so each dot
-// product is unchanged.  The per-token fp8 scale and
-// the per-32-dim e8m0 scales are applied to the fp32 partial sums, then the
-// page max is a shuffle reduction over the 16 tokens of the tile.
+// product is unchanged.  The per-token fp8 scale and the per-32-dim e8m0
+// scales are applied to the fp32 partial sums, then the page max is a shuffle
+// reduction over the 16 tokens of the tile.
 #include <algorithm>
 
 #include "common.cuh"
@@ -58,7 +59,6 @@ struct KeyFmt<kFp8KeysE4m3Q> {
   static constexpr int kField = kFp8IndexField;
   static constexpr int kStages = 4;
 };
-
 template <int KEY>
 constexpr int smem_bytes(int stages) {
   return stages * KeyFmt<KEY>::kField + stages * 8;

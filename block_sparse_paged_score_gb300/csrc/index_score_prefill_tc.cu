@@ -250,24 +250,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int et = tid - 32;           // 0..255
+    const int et = tid - 32;           // 0..255: the key whose scale this thread stages
     const int col0 = 128 * ((warp - 1) >> 2);  // this warp's half of the 256 columns
+    // fp32 scale of key `et` of tile jj (0 for a missing block)
+    auto scale_of = [&](int jj) -> float {
+      const int blk = kb0 + 2 * jj + (et >> 7);
+      if (blk >= kb0 + nb) return 0.f;
+      const int bid = s_bid[blk - kb0];
+      return bid < 0 ? 0.f
+                     : *reinterpret_cast<const float*>(p.idx_base + static_cast<int64_t>(bid) * p.block_stride +
+                                                       kFp8IndexScaleOff + (et & 127) * 4);
+    };
+    float scale_next = scale_of(0);  // loaded one tile ahead of use
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
       // stage the fp32 scales of the tile's 256 keys (the previous user of
       // this buffer, tile j-2, is finished: every epilogue thread passed the
-      // barrier below for tile j-1)
-      for (int i = et; i < 256; i += 32 * kEpiWarps) {
-        const int blk = kb0 + 2 * j + (i >> 7);
-        float s = 0.f;
-        if (blk < kb0 + nb) {
-          const int bid = s_bid[blk - kb0];
-          if (bid >= 0)
-            s = *reinterpret_cast<const float*>(p.idx_base + static_cast<int64_t>(bid) * p.block_stride +
-                                                kFp8IndexScaleOff + (i & 127) * 4);
-        }
-        sm.scales[buf * 256 + i] = s;
-      }
+      // barrier below for tile j-1); the next tile's load is in flight while
+      // this tile is processed
+      sm.scales[buf * 256 + et] = scale_next;
+      if (j + 1 < ntiles) scale_next = scale_of(j + 1);
       epi_barrier();
       mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -278,16 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         const int c0 = col0 + 32 * cc;
         tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * 256 + c0, v);
+        const float* sc = sm.scales + buf * 256 + c0;
+        if (key0 + c0 + 32 <= L) {  // every key of the chunk is inside the row's causal length
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float m = -INFINITY;
+          for (int hh = 0; hh < 2; ++hh) {
+            float m = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = c0 + 16 * hh + c;
-            const float x = v[16 * hh + c] * sm.scales[buf * 256 + col];
-            m = key0 + col < L ? fmaxf(m, x) : m;
+            for (int c = 0; c < 16; ++c) m = fmaxf(m, v[16 * hh + c] * sc[16 * hh + c]);
+            pv[2 * cc + hh] = m;
           }
-          pv[2 * cc + hh] = m;
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int col = c0 + 16 * hh + c;
+              const float x = v[16 * hh + c] * sc[16 * hh + c];
+              m = key0 + col < L ? fmaxf(m, x) : m;
+            }
+            pv[2 * cc + hh] = m;
+          }
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

@@ -84,6 +84,8 @@ typedef enum {
 
 /* top-k flags */
 #define BSP_FORCE_TAIL 1 /* the tail page of every row is always selected */
+/* decode-step flag: reuse another layer's selection (see bsp_sparse_decode_step) */
+#define BSP_REUSE_SELECTION 2
 
 /* ------------------------------------------------------------------------
  * K/V cache descriptor.
@@ -332,6 +334,14 @@ bsp_status bsp_sparse_pa_prefill(const bsp_kv_cache* kv, const void* q, int32_t 
  * `events` (nullable) receives 5 cudaEventRecord calls on `stream`: before
  * the write, before scoring, before the selection, before the attention, and
  * at the end.
+ *
+ * With BSP_REUSE_SELECTION in `flags` the step attends with the sparse_bt /
+ * sparse_ctx already in the arguments -- the selection of another layer
+ * that shares this layer's tokens (ROCm/ATOM PR 2962: layers without an
+ * indexer reuse a previous layer's top-k) -- and skips the index-key write,
+ * the row lengths, the scoring and the selection.  idx, idx_k_new, idx_q,
+ * idx_q_cast, row_seq, row_len, scores and topk_idx are then unused (NULL is
+ * fine); the three middle events mark the same point.
  * ---------------------------------------------------------------------- */
 typedef struct bsp_decode_step_args {
   const bsp_kv_cache* kv;
@@ -357,7 +367,7 @@ typedef struct bsp_decode_step_args {
   int32_t bt_stride;
   int32_t max_pages;
   int32_t k_pages;
-  int32_t flags;              /* BSP_FORCE_TAIL */
+  int32_t flags;              /* BSP_FORCE_TAIL, BSP_REUSE_SELECTION */
   float sm_scale;
   /* outputs and scratch (caller-owned device memory) */
   int32_t* row_seq;           /* [rows] */

@@ -285,6 +285,45 @@ def test_decode_step_matches_ops(bsp, name):
     assert st.dev_err.item() == 0
 
 
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx"])
+def test_decode_step_reuses_another_layers_selection(bsp, name):
+    """BSP_REUSE_SELECTION: a second layer's step (its own K/V cache, no
+    index cache) attends with the first layer's sparse table; it equals the
+    attention call on that table bit for bit, and writes the layer's new
+    tokens."""
+    import ctypes as C
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides(name)
+    st = step.DecodeStep(w, g.kv, g.idx, g.block_table)
+    k, v, ik, slot = w.step_tokens()
+    st.run(g.t(k), g.t(v), g.t(ik), g.t(slot), g.q_bf16, g.idx_q_bf16, g.t(w.decode_lens))
+    # layer 2: the same shapes and tokens, other values
+    w2 = W.Workload(dict(MINI[name], seed=MINI[name]["seed"] + 500))
+    g2 = GpuSide(w2)
+    k2, v2, _, slot2 = w2.step_tokens()
+    q2, _ = w2.queries()
+    q2 = g2.t(q2)
+    st2 = step.DecodeStep(w2, g2.kv, g2.idx, g2.block_table)
+    a = st2.args
+    a.idx = C.cast(None, C.POINTER(bsp.IndexCacheDesc))
+    a.flags = bsp.REUSE_SELECTION
+    a.sparse_bt, a.sparse_ctx = st.sparse_bt.data_ptr(), st.sparse_ctx.data_ptr()
+    a.row_seq = a.row_len = a.scores = a.topk_idx = None
+    idx_before = g2.idx.buffer.clone()
+    st2.run(g2.t(k2), g2.t(v2), g2.t(k2), g2.t(slot2), q2, q2, g2.t(w2.decode_lens))
+    ref = bsp.sparse_pa_decode(g2.kv, bsp.cast_e4m3(q2) if w2.q_dtype == W.FP8 else q2, w2.q_dtype, w2.hq,
+                               st.sparse_bt, st.sparse_ctx, w2.k_pages, SM_SCALE)
+    torch.cuda.synchronize()
+    assert st2.dev_err.item() == 0
+    assert torch.equal(st2.out, ref)
+    assert torch.equal(g2.idx.buffer, idx_before)  # no index-key write
+    # the new tokens were written into layer 2's cache: the writer's own call gives the same bytes
+    kv_copy = g2.kv.buffer.clone()
+    bsp.kv_page_write(g2.kv, g2.idx, g2.t(k2), g2.t(v2), g2.t(k2), g2.t(slot2))
+    torch.cuda.synchronize()
+    assert torch.equal(g2.kv.buffer, kv_copy)
+
+
 def test_device_errors_are_flagged_not_faulted(bsp):
     w, o, g = sides("fp8")
     rows = 4
