@@ -267,7 +267,7 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
   if (k_pages > 2048 || max_pages > 65536) return BSP_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_pages) > static_cast<int64_t>(bt_stride) * 8) return BSP_ERR_INVALID_ARG;
   if (num_rows == 0) return BSP_OK;
-  if (!scores || !row_seq || !row_len || !block_table || !topk_idx || !sparse_bt || !sparse_ctx)
+  if (!scores || !row_seq || !row_len || !block_table || !topk_idx || !sparse_bt || !sparse_ctx || !al(scores, 16))
     return BSP_ERR_INVALID_ARG;
   TopkParams p{};
   p.scores = scores;

@@ -7,7 +7,7 @@
 //   scores[i, p] = max_{t in page p, t < L_i} S[i, t],  -inf past ceil(L_i/16)
 //
 // One CTA = one tile of 128 consecutive query rows of one chunk (a chunk is
-// a run of query tokens of one sequence) x a range of 16 key blocks (2048
+// a run of query tokens of one sequence) x a range of 64 key blocks (8192
 // keys).  Warp 0, lane 0 is the producer and the MMA issuer:
 //   - the query tile and each pair of key blocks arrive by 2-D TMA tensor
 //     loads with 128-byte swizzle (box 128 rows x 128 B) on mbarriers; key
@@ -19,7 +19,8 @@
 //     tcgen05.commit releases the key stage and signals the accumulator.
 // Warps 1..8 are the epilogue: warp w reads TMEM lanes 32*(w%4).. (its
 // quarter) and half of the 256 columns with tcgen05.ld, multiplies by the
-// per-token fp32 scales (staged in shared memory per tile), masks keys at
+// per-token fp32 scales (which the producer copies per tile into one of two
+// shared-memory slots with a 1-D TMA, next to the accumulator), masks keys at
 // or past the row's causal length, max-pools 16 keys into a page score and
 // stores 8 pages per row per tile.  Accumulator double-buffering lets the
 // MMAs of the next tile run under the epilogue of this one.
@@ -34,7 +35,7 @@ namespace bsp {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kKeyBlocksPerCta = 16;
+constexpr int kKeyBlocksPerCta = 64;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (1 + kEpiWarps);
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 B
@@ -100,10 +101,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void epi_barrier() {
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -129,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_empty = sm.bars + 1 + kStages;
   uint64_t* acc_full = sm.bars + 1 + 2 * kStages;
   uint64_t* acc_empty = sm.bars + 3 + 2 * kStages;
+  uint64_t* scale_full = sm.bars + 5 + 2 * kStages;  // [2]: a tile's key scales landed in sm.scales
   __shared__ int s_tok0, s_tok1, s_lmax, s_seq;
   __shared__ int s_bid[kKeyBlocksPerCta];  // the key range's block ids (-1: missing)
 
@@ -163,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * kEpiWarps);
+      mbar_init(&scale_full[i], 1);
     }
     mbar_fence_init();
   }
@@ -235,6 +234,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStages, buf = j & 1;
         mbar_wait(&b_full[st], (j / kStages) & 1, p.err);
         mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
+        // the tile's fp32 key scales (512 B per block) into this buffer's
+        // scale slots: the epilogue of tile j-2 has released them
+        {
+          fence_proxy_async();
+          uint32_t bytes = 0;
+          for (int h = 0; h < 2; ++h) {
+            const int blk = kb0 + 2 * j + h;
+            if (blk < kb0 + nb && s_bid[blk - kb0] >= 0) bytes += 512;
+          }
+          mbar_arrive_expect_tx(&scale_full[buf], bytes);
+          for (int h = 0; h < 2; ++h) {
+            const int blk = kb0 + 2 * j + h;
+            if (blk < kb0 + nb && s_bid[blk - kb0] >= 0)
+              bulk_g2s(sm.scales + buf * 256 + 128 * h,
+                       p.idx_base + static_cast<int64_t>(s_bid[blk - kb0]) * p.block_stride + kFp8IndexScaleOff, 512,
+                       &scale_full[buf]);
+          }
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(sm.b + st * 2 * kTileBytes);
 #pragma unroll
@@ -250,27 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const int et = tid - 32;           // 0..255: the key whose scale this thread stages
     const int col0 = 128 * ((warp - 1) >> 2);  // this warp's half of the 256 columns
-    // fp32 scale of key `et` of tile jj (0 for a missing block)
-    auto scale_of = [&](int jj) -> float {
-      const int blk = kb0 + 2 * jj + (et >> 7);
-      if (blk >= kb0 + nb) return 0.f;
-      const int bid = s_bid[blk - kb0];
-      return bid < 0 ? 0.f
-                     : *reinterpret_cast<const float*>(p.idx_base + static_cast<int64_t>(bid) * p.block_stride +
-                                                       kFp8IndexScaleOff + (et & 127) * 4);
-    };
-    float scale_next = scale_of(0);  // loaded one tile ahead of use
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
-      // stage the fp32 scales of the tile's 256 keys (the previous user of
-      // this buffer, tile j-2, is finished: every epilogue thread passed the
-      // barrier below for tile j-1); the next tile's load is in flight while
-      // this tile is processed
-      sm.scales[buf * 256 + et] = scale_next;
-      if (j + 1 < ntiles) scale_next = scale_of(j + 1);
-      epi_barrier();
+      // the tile's key scales (a missing block leaves stale but finite
+      // scales: its keys lie past every row's length and are masked)
+      mbar_wait(&scale_full[buf], (j >> 1) & 1, p.err);
       mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       float pv[8];

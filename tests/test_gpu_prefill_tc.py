@@ -1,6 +1,6 @@
 """Parity of the tcgen05 prefill index scorer with the oracle (GPU required):
 fp8 index cache, e4m3 index queries, chunks of consecutive query tokens with
-causal lengths, partial 128-row tiles, several 2048-key ranges and pad rows."""
+causal lengths, partial 128-row tiles, several 8192-key ranges and pad rows."""
 import numpy as np
 import pytest
 import torch
@@ -20,6 +20,10 @@ CASES = {
     "ranges": dict(name="pre-ranges", seed=22, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
                    hkv=1, group=16, k_pages=32, q_len=1, decode_lens=[5000],
                    prefill_chunks=[(3000, 700), (5200, 1100), (128, 128)], pad_seqs=2, pad_q_len=4),
+    # contexts past 8192 keys: several key ranges per query tile
+    "wide": dict(name="pre-wide", seed=23, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
+                 hkv=1, group=16, k_pages=32, q_len=1, decode_lens=[100],
+                 prefill_chunks=[(9100, 300), (17000, 260)], pad_seqs=1, pad_q_len=4),
 }
 
 
