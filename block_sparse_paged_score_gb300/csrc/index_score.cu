@@ -72,16 +72,6 @@ __device__ __forceinline__ int frag_dim(int m, int t) {
   return 8 * (t + 4 * (m >> 1)) + 4 * (m & 1);
 }
 
-// D (16x8 f32) += A (16x32 e4m3, row) * B (32x8 e4m3, col)
-__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off, float (&v)[4]) {
   if (q_dtype == BSP_BF16) {
     const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(q) + off);
