@@ -185,10 +185,11 @@ bsp_status bsp_row_lengths_prefill(const int32_t* query_req_id, const int32_t* q
   return st;
 }
 
-bsp_status bsp_index_score(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
-                           const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
-                           const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
-                           float* scores, int32_t* dev_err, bsp_stream_t stream) {
+// seq_is_group: the decode step's own rows, where query group g is sequence g
+static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
+                                   const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
+                                   const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
+                                   float* scores, int32_t* dev_err, bsp_stream_t stream, int32_t seq_is_group) {
   bsp_status st = check_idx(idx);
   if (st != BSP_OK) return st;
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1) return BSP_ERR_INVALID_ARG;
@@ -216,9 +217,18 @@ bsp_status bsp_index_score(const bsp_index_cache* idx, const void* idx_q, int32_
   p.max_pages = max_pages;
   p.scores = scores;
   p.err = dev_err;
+  p.seq_is_group = seq_is_group;
   st = cuda_status(launch_index_score(p, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
   if (st == BSP_OK) ++g_launches;
   return st;
+}
+
+bsp_status bsp_index_score(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
+                           const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
+                           const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
+                           float* scores, int32_t* dev_err, bsp_stream_t stream) {
+  return index_score_impl(idx, idx_q, q_dtype, block_table, bt_stride, row_seq, row_len, num_rows, q_group,
+                          max_pages, scores, dev_err, stream, 0);
 }
 
 bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
@@ -258,10 +268,11 @@ bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q
   return st;
 }
 
-bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
-                           const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
-                           int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt, int32_t* sparse_ctx,
-                           bsp_stream_t stream) {
+// rows_per_seq > 0: row r belongs to sequence r / rows_per_seq (the decode step's own rows)
+static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
+                            const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
+                            int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt,
+                            int32_t* sparse_ctx, bsp_stream_t stream, int32_t rows_per_seq) {
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1 || k_pages < 1 || !valid_dtype(kv_dtype))
     return BSP_ERR_INVALID_ARG;
   if (k_pages > 2048 || max_pages > 65536) return BSP_ERR_UNSUPPORTED;
@@ -283,9 +294,18 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
   p.topk_idx = topk_idx;
   p.sparse_bt = sparse_bt;
   p.sparse_ctx = sparse_ctx;
+  p.rows_per_seq = rows_per_seq;
   bsp_status st = cuda_status(launch_topk_select(p, reinterpret_cast<cudaStream_t>(stream)));
   if (st == BSP_OK) ++g_launches;
   return st;
+}
+
+bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
+                           const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
+                           int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt, int32_t* sparse_ctx,
+                           bsp_stream_t stream) {
+  return topk_impl(scores, num_rows, max_pages, row_seq, row_len, block_table, bt_stride, kv_dtype, k_pages, flags,
+                   topk_idx, sparse_bt, sparse_ctx, stream, 0);
 }
 
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group) {
@@ -445,14 +465,17 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   if ((st = cuda_status(launch_decode_prep(pp, s))) != BSP_OK) return st;
   ++g_launches;
   mark(1);
+  // the step's rows are decode-ordered (row_seq = token / q_len, as the prep
+  // kernel writes it): the scorer and the selector find a row's sequence
+  // without reading row_seq first
   if (!reuse &&
-      (st = bsp_index_score(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
-                            a->q_len, a->max_pages, a->scores, a->dev_err, stream)) != BSP_OK)
+      (st = index_score_impl(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
+                             a->q_len, a->max_pages, a->scores, a->dev_err, stream, 1)) != BSP_OK)
     return st;
   mark(2);
-  if (!reuse && (st = bsp_topk_select(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table,
-                                      a->bt_stride, a->kv->dtype, a->k_pages, a->flags & BSP_FORCE_TAIL, a->topk_idx,
-                                      a->sparse_bt, a->sparse_ctx, stream)) != BSP_OK)
+  if (!reuse && (st = topk_impl(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
+                                a->kv->dtype, a->k_pages, a->flags & BSP_FORCE_TAIL, a->topk_idx, a->sparse_bt,
+                                a->sparse_ctx, stream, a->q_len * hkv)) != BSP_OK)
     return st;
   mark(3);
   if ((st = bsp_sparse_pa_decode(a->kv, q, a->q_dtype, a->num_q_heads, a->sparse_bt, a->sparse_ctx, rows, a->k_pages,

@@ -101,9 +101,15 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   const int tok0 = group * p.q_group;
   const int ntok = min(p.q_group, p.num_tokens - tok0);
   const int max_len = p.max_pages * kPage;
+  const int blk0 = chunk * p.blocks_per_chunk;
 
   pdl_wait();  // row lengths come from the kernel before
   pdl_trigger();
+  // decode-ordered rows: the chunk's block ids load alongside the rows'
+  // lengths instead of after them (entries past the context go unused)
+  int32_t bid_early = 0;
+  if (p.seq_is_group && tid < p.blocks_per_chunk && (blk0 + tid) * kPagesPerSide < p.max_pages)
+    bid_early = p.block_table[static_cast<int64_t>(group) * p.bt_stride + blk0 + tid];
   if (tid < 8) {
     int L = 0, r = -1;
     if (tid < ntok) {
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
     s_row[tid] = r;
   }
   if (tid == 0) {
-    s_seq = p.row_seq[tok0 * p.hidx + h];
+    s_seq = p.seq_is_group ? group : p.row_seq[tok0 * p.hidx + h];
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
@@ -125,7 +131,6 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) lmax = max(lmax, s_len[i]);
   const int seq = s_seq;
-  const int blk0 = chunk * p.blocks_per_chunk;
   const int nb = max(0, min(p.blocks_per_chunk, (lmax + kBlock - 1) / kBlock - blk0));
   const int page_end = min((blk0 + p.blocks_per_chunk) * kPagesPerSide, p.max_pages);
 
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   }
   if (nb == 0) return;
   if (tid < nb) {
-    int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + tid];
+    int bid = p.seq_is_group ? bid_early : p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + tid];
     if (bid < 0 || bid >= p.num_blocks) {
       set_err(p.err, BSP_DEVERR_BLOCK_ID);
       bid = 0;
@@ -329,18 +334,21 @@ int occupancy_key(int stages) {
 // CTAs per SM.  `max_blocks` counts every group at the batch's longest
 // context; CTAs past a shorter sequence only write -inf and retire at once.
 constexpr double kStartBlocks = 1.5;
+#ifndef BSP_IDX_MIN_CB
+#define BSP_IDX_MIN_CB 1
+#endif
 
 template <int KEY>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
   double best = 0.0;
-  for (int cb = 1; cb <= 32; ++cb) {
+  for (int cb = BSP_IDX_MIN_CB; cb <= 32; ++cb) {
     const int stages = std::min(cb, KeyFmt<KEY>::kStages);
     const int64_t resident = static_cast<int64_t>(occupancy_key<KEY>(stages)) * num_sms;
     const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
     const int64_t waves = (ctas + resident - 1) / resident;
     const double cost = static_cast<double>(waves) * (cb + kStartBlocks);
-    if (cb == 1 || cost < best) {
+    if (cb == BSP_IDX_MIN_CB || cost < best) {
       best = cost;
       p.blocks_per_chunk = cb;
       p.stages = stages;

@@ -91,6 +91,7 @@ struct IndexScoreParams {
   const int32_t* row_len;
   int32_t num_rows, num_tokens, q_group, max_pages;
   int32_t blocks_per_chunk, num_groups, stages;  // filled by the launcher
+  int32_t seq_is_group;  // 1: rows are decode-ordered, group g is sequence g (no row_seq lookup first)
   float* scores;
   int32_t* err;
 };
@@ -104,6 +105,7 @@ struct TopkParams {
   const int32_t* block_table;
   int32_t bt_stride, id_mul;  // id = block * id_mul + p % 8
   int32_t k_pages, force_tail;
+  int32_t rows_per_seq;  // > 0: row r belongs to sequence r / rows_per_seq (no row_seq lookup first)
   int32_t* topk_idx;
   int32_t* sparse_bt;
   int32_t* sparse_ctx;

@@ -529,21 +529,25 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
   // first pages are fetched
   const QRaw qraw =
       load_q_raw<KV>(p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, warp, lane);
+  // this warp's page ids, 32 at a time, loaded together ahead of use: lane j
+  // holds the id of the warp's page 32*c + j (the ring issues its TMA copies
+  // from these without a dependent global load).  The first 32 are loaded
+  // alongside the row's context length, over the split's whole page range
+  // (entries past the context are never used).
+  const int p0 = split * p.pages_per_split;
+  const int pmax = min(p0 + p.pages_per_split, p.k_pages);  // the split's pages, whatever the context
+  const int32_t* sbt = p.sparse_bt + static_cast<int64_t>(row) * p.k_pages;
+  int32_t my_id = 0;
+  int id_chunk = 0;
+  if (p0 + warp + 4 * lane < pmax) my_id = sbt[p0 + warp + 4 * lane];
   const int ctx = min(max(p.sparse_ctx[row], 0), p.k_pages * kPage);
   const int npages = (ctx + kPage - 1) / kPage;
-  const int p0 = split * p.pages_per_split, p1 = min(p0 + p.pages_per_split, npages);
+  const int p1 = min(pmax, npages);
   const int nw = p1 > p0 + warp ? (p1 - p0 - warp + 3) / 4 : 0;
-  const int32_t* sbt = p.sparse_bt + static_cast<int64_t>(row) * p.k_pages;
   uint8_t* wring = smem + warp * R * SB;
   uint64_t* wbar = bars + warp * R;
   uint8_t* wdq = smem + 4 * R * SB + warp * DQ;
 
-  // this warp's page ids, 32 at a time, loaded together ahead of use: lane j
-  // holds the id of the warp's page 32*c + j (the ring issues its TMA copies
-  // from these without a dependent global load)
-  int32_t my_id = 0;
-  int id_chunk = 0;
-  if (lane < nw) my_id = sbt[p0 + warp + 4 * lane];
   auto id_of = [&](int j) -> int32_t {  // warp-uniform j
     if ((j >> 5) != id_chunk) {
       id_chunk = j >> 5;

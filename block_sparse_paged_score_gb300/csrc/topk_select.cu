@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) topk_select_kernel(TopkParams p) {
     }
   }
   int sel_before = block_exclusive_scan(n_sel, s_warp, tot);
-  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  const int64_t bt_row = static_cast<int64_t>(p.rows_per_seq > 0 ? r / p.rows_per_seq : p.row_seq[r]) * p.bt_stride;
   {
     int eqr = eq_before, pos = sel_before;
     int cur_blk = -1, cur_id = 0;  // this thread's pages are contiguous: few distinct blocks
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
   // independent loads first: the row's length and sequence, every score of
   // the row and its block ids (valid memory whatever the length)
   const int L = min(max(p.row_len[r], 0), max_len);
-  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  const int64_t bt_row = static_cast<int64_t>(p.rows_per_seq > 0 ? r / p.rows_per_seq : p.row_seq[r]) * p.bt_stride;
   const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
   float sv[KPL];
 #pragma unroll
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   const int first = tid * KPT;
   const int nblk = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
   const int b0 = first / kPagesPerSide;
-  const int64_t bt_row = static_cast<int64_t>(p.row_seq[r]) * p.bt_stride;
+  const int64_t bt_row = static_cast<int64_t>(p.rows_per_seq > 0 ? r / p.rows_per_seq : p.row_seq[r]) * p.bt_stride;
   int32_t ids[NB];
 #pragma unroll
   for (int k = 0; k < NB; ++k) ids[k] = b0 + k < nblk ? p.block_table[bt_row + b0 + k] * p.id_mul : 0;
