@@ -334,21 +334,18 @@ int occupancy_key(int stages) {
 // CTAs per SM.  `max_blocks` counts every group at the batch's longest
 // context; CTAs past a shorter sequence only write -inf and retire at once.
 constexpr double kStartBlocks = 1.5;
-#ifndef BSP_IDX_MIN_CB
-#define BSP_IDX_MIN_CB 1
-#endif
 
 template <int KEY>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
   double best = 0.0;
-  for (int cb = BSP_IDX_MIN_CB; cb <= 32; ++cb) {
+  for (int cb = 1; cb <= 32; ++cb) {
     const int stages = std::min(cb, KeyFmt<KEY>::kStages);
     const int64_t resident = static_cast<int64_t>(occupancy_key<KEY>(stages)) * num_sms;
     const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
     const int64_t waves = (ctas + resident - 1) / resident;
     const double cost = static_cast<double>(waves) * (cb + kStartBlocks);
-    if (cb == BSP_IDX_MIN_CB || cost < best) {
+    if (cb == 1 || cost < best) {
       best = cost;
       p.blocks_per_chunk = cb;
       p.stages = stages;

@@ -78,6 +78,9 @@ constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 #ifndef BSP_PA_FP8_MIN_CTAS
 #define BSP_PA_FP8_MIN_CTAS 4
 #endif
+#ifndef BSP_PA_MX_MIN_CTAS
+#define BSP_PA_MX_MIN_CTAS 2
+#endif
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
   static constexpr int kRing = BSP_PA_FP8_RING, kRingMax = 6, kSlot = 4096, kDeq = 0, kMinCtas = BSP_PA_FP8_MIN_CTAS;
@@ -89,7 +92,7 @@ struct PaFmt<BSP_BF16> {
 template <>
 struct PaFmt<BSP_MXFP4> {
   // K data 1024 | K scales 64 | V data 1024 | V scales 64
-  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
+  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = BSP_PA_MX_MIN_CTAS;
 };
 
 // shared memory: the rings (and MXFP4 dequant pages) during the page loop,
@@ -152,29 +155,31 @@ __device__ __forceinline__ void mx_page_to_bf16(const uint8_t* slot, uint8_t* dq
       *reinterpret_cast<uint4*>(dq + (hf * 8 + j) * 256 + tk * 16) = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
-  {  // V: lane = dims 4*lane..+3, all 16 tokens
+  {  // V: lane = dims 4*lane..+3; 8 tokens at a time
     const uint8_t* vd = slot + 1088;
     const uint8_t* vs = slot + 2112;
-    float v[16][4];
 #pragma unroll
-    for (int tk = 0; tk < 16; ++tk) {
-      const uint32_t two = *reinterpret_cast<const uint16_t*>(vd + tk * 64 + 2 * lane);
-      const float s = e8m0_to_float(vs[tk * 4 + (lane >> 3)]);
-      const float2 f0 = f16x2_to_float2(e2m1x2_to_f16x2(two & 0xFF));
-      const float2 f1 = f16x2_to_float2(e2m1x2_to_f16x2(two >> 8));
-      v[tk][0] = f0.x * s, v[tk][1] = f0.y * s, v[tk][2] = f1.x * s, v[tk][3] = f1.y * s;
-    }
+    for (int th = 0; th < 2; ++th) {
+      float v[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int k = 0; k < 8; ++k) {
+        const int tk = 8 * th + k;
+        const uint32_t two = *reinterpret_cast<const uint16_t*>(vd + tk * 64 + 2 * lane);
+        const float s = e8m0_to_float(vs[tk * 4 + (lane >> 3)]);
+        const float2 f0 = f16x2_to_float2(e2m1x2_to_f16x2(two & 0xFF));
+        const float2 f1 = f16x2_to_float2(e2m1x2_to_f16x2(two >> 8));
+        v[k][0] = f0.x * s, v[k][1] = f0.y * s, v[k][2] = f1.x * s, v[k][3] = f1.y * s;
+      }
 #pragma unroll
-      for (int th = 0; th < 2; ++th) {
+      for (int i = 0; i < 4; ++i) {
         uint4 w;
-        w.x = pack_bf16x2(v[8 * th + 0][i], v[8 * th + 1][i]);
-        w.y = pack_bf16x2(v[8 * th + 2][i], v[8 * th + 3][i]);
-        w.z = pack_bf16x2(v[8 * th + 4][i], v[8 * th + 5][i]);
-        w.w = pack_bf16x2(v[8 * th + 6][i], v[8 * th + 7][i]);
+        w.x = pack_bf16x2(v[0][i], v[1][i]);
+        w.y = pack_bf16x2(v[2][i], v[3][i]);
+        w.z = pack_bf16x2(v[4][i], v[5][i]);
+        w.w = pack_bf16x2(v[6][i], v[7][i]);
         *reinterpret_cast<uint4*>(dq + 4096 + th * 2048 + (4 * lane + i) * 16) = w;
       }
+    }
   }
 }
 
