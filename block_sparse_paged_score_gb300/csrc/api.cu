@@ -321,7 +321,7 @@ size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, i
 static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
                                    const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
                                    int32_t k_pages, float sm_scale, void* out, void* ws, size_t ws_bytes,
-                                   int32_t* dev_err, bsp_stream_t stream, bool decode) {
+                                   int32_t* dev_err, bsp_stream_t stream, bool decode, bool q_early = false) {
   bsp_status st = check_kv(kv);
   if (st != BSP_OK) return st;
   if (num_rows < 0 || k_pages < 1 || num_q_heads < 1) return BSP_ERR_INVALID_ARG;
@@ -350,6 +350,7 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   p.sm_scale = sm_scale;
   p.out = out;
   p.err = dev_err;
+  p.q_early = q_early;
   if (decode) {
     const PaPlan plan = sparse_pa_plan(kv->dtype, num_rows, k_pages, device_sms());
     p.nsplit = plan.nsplit;
@@ -478,8 +479,11 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
                                 a->sparse_ctx, stream, a->q_len * hkv)) != BSP_OK)
     return st;
   mark(3);
-  if ((st = bsp_sparse_pa_decode(a->kv, q, a->q_dtype, a->num_q_heads, a->sparse_bt, a->sparse_ctx, rows, a->k_pages,
-                                 a->sm_scale, a->out, a->ws, a->ws_bytes, a->dev_err, stream)) != BSP_OK)
+  // the attention's queries were written two launches back (or are the
+  // caller's bf16 input) unless the prep kernel right before it cast them
+  const bool q_early = !(reuse && a->q_dtype == BSP_FP8_E4M3);
+  if ((st = sparse_pa_common(a->kv, q, a->q_dtype, a->num_q_heads, a->sparse_bt, a->sparse_ctx, rows, a->k_pages,
+                             a->sm_scale, a->out, a->ws, a->ws_bytes, a->dev_err, stream, true, q_early)) != BSP_OK)
     return st;
   mark(4);
   return BSP_OK;

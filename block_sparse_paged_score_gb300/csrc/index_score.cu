@@ -326,25 +326,28 @@ int occupancy_key(int stages) {
 }
 
 // Blocks per CTA (cb) and ring depth.  Each CTA pays a fixed start (row
-// lengths, block ids, the first copy) of about kStartBlocks blocks' worth of
-// streaming; CTAs run in waves of `resident`.  The plan minimises
-// waves * (cb + kStartBlocks) over cb = 1..32 -- whole waves, without
-// splitting a sequence's blocks finer than it pays for.  The ring holds
-// min(cb, kStages) fields, so a one-block CTA needs one stage and packs more
-// CTAs per SM.  `max_blocks` counts every group at the batch's longest
-// context; CTAs past a shorter sequence only write -inf and retire at once.
-constexpr double kStartBlocks = 1.5;
+// lengths, block ids, the first copy) that costs about as long as streaming
+// kStartBytes; CTAs run in waves of `resident`.  The plan minimises
+// waves * (cb + kStartBytes / field bytes) over cb = 1..32 -- whole waves,
+// without splitting a sequence's blocks finer than it pays for.  The start
+// is a time, so it is worth more of the small MXFP4 fields than of the fp8
+// ones.  The ring holds min(cb, kStages) fields, so a one-block CTA needs one
+// stage and packs more CTAs per SM.  `max_blocks` counts every group at the
+// batch's longest context; CTAs past a shorter sequence only write -inf and
+// retire at once.
+constexpr double kStartBytes = 1.5 * kFp8IndexField;
 
 template <int KEY>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
+  const double start_blocks = kStartBytes / KeyFmt<KEY>::kField;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {
     const int stages = std::min(cb, KeyFmt<KEY>::kStages);
     const int64_t resident = static_cast<int64_t>(occupancy_key<KEY>(stages)) * num_sms;
     const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
     const int64_t waves = (ctas + resident - 1) / resident;
-    const double cost = static_cast<double>(waves) * (cb + kStartBlocks);
+    const double cost = static_cast<double>(waves) * (cb + start_blocks);
     if (cb == 1 || cost < best) {
       best = cost;
       p.blocks_per_chunk = cb;

@@ -129,6 +129,7 @@ struct SparsePaParams {
   int32_t nsplit, pages_per_split;
   int32_t cluster;  // 2..8: the row's splits form a cluster and merge on chip
   int32_t ring;     // pages in flight per warp
+  int32_t q_early;  // 1: q was written before the kernel launched ahead of this one (load it before the wait)
   int32_t* err;
 };
 // split plan shared by the launcher and the workspace query

@@ -526,14 +526,19 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
     for (int i = 0; i < 4 * R; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
   }
+  const int64_t q_off = (token * hq + static_cast<int64_t>(h) * p.group) * kDim;
+  QRaw qraw;
+  if (p.q_early) {  // the queries do not come from the kernel before: stage them before waiting
+    qraw = load_q_raw<KV>(p.q, p.q_dtype, q_off, p.group, warp, lane);
+    store_q_raw<KV>(qs, qraw, p.q_dtype, warp, lane);
+  }
   __syncthreads();
-  pdl_wait();  // the sparse table and the queries come from earlier kernels
+  pdl_wait();  // the sparse table (and the queries, unless staged) come from earlier kernels
   pdl_trigger();
 
   // the queries' loads go out first; they land while the page ids and the
   // first pages are fetched
-  const QRaw qraw =
-      load_q_raw<KV>(p.q, p.q_dtype, (token * hq + static_cast<int64_t>(h) * p.group) * kDim, p.group, warp, lane);
+  if (!p.q_early) qraw = load_q_raw<KV>(p.q, p.q_dtype, q_off, p.group, warp, lane);
   // this warp's page ids, 32 at a time, loaded together ahead of use: lane j
   // holds the id of the warp's page 32*c + j (the ring issues its TMA copies
   // from these without a dependent global load).  The first 32 are loaded
@@ -566,8 +571,10 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
     if (lane == 0 && i < nw) issue_page<KV>(p, id, h, wring + i * SB, &wbar[i]);
   }
 
-  store_q_raw<KV>(qs, qraw, p.q_dtype, warp, lane);
-  __syncthreads();
+  if (!p.q_early) {
+    store_q_raw<KV>(qs, qraw, p.q_dtype, warp, lane);
+    __syncthreads();
+  }
 
   PaState a;
   pa_state_init(a);

@@ -328,8 +328,15 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   __shared__ int s_above;
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
-  pdl_wait();  // scores come from the kernel before
-  pdl_trigger();
+  // Inside the decode step (rows_per_seq > 0) the row lengths come from the
+  // step's first kernel, done before the scorer started: only the scores
+  // need the wait, so the lengths, the unused tail of the outputs and the
+  // block ids go first.  Every CTA still waits before it exits.
+  const bool in_step = p.rows_per_seq > 0;
+  if (!in_step) {
+    pdl_wait();  // scores (and the row lengths) come from earlier kernels
+    pdl_trigger();
+  }
   const int max_len = p.max_pages * kPage;
   const int L = min(max(p.row_len[r], 0), max_len);
   const int n = (L + kPage - 1) / kPage;
@@ -339,6 +346,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   for (int m = kk + tid; m < p.k_pages; m += kCtaThreads) ti[m] = bt[m] = -1;
   if (kk == 0) {
     if (tid == 0) p.sparse_ctx[r] = 0;
+    if (in_step) pdl_wait();
     return;
   }
   const int n_cand = p.force_tail ? n - 1 : n;
@@ -355,6 +363,10 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   int32_t ids[NB];
 #pragma unroll
   for (int k = 0; k < NB; ++k) ids[k] = b0 + k < nblk ? p.block_table[bt_row + b0 + k] * p.id_mul : 0;
+  if (in_step) {
+    pdl_wait();  // the scores
+    pdl_trigger();
+  }
   const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
   uint32_t key[KPT];
 #pragma unroll

@@ -285,6 +285,45 @@ def test_decode_step_matches_ops(bsp, name):
     assert st.dev_err.item() == 0
 
 
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2"])
+def test_decode_step_with_tokens_written_into_older_blocks(bsp, name):
+    """New tokens need not be a sequence's last positions: here they also go
+    to the first position of each sequence's first block.  The step must
+    score and attend over the freshly written keys, exactly as the separate
+    calls made after the write do, and the oracle agrees on page 0."""
+    from block_sparse_paged_score_gb300 import step
+    w = W.Workload(dict(MINI[name], seed=MINI[name]["seed"] + 900))
+    g = GpuSide(w)
+    k, v, ik, slot = w.step_tokens()
+    rng = np.random.default_rng(7)
+    seqs = [s for s in range(w.num_decode) if w.decode_lens[s] > w.q_len]  # position 0 is not a step token
+    extra = np.array([w.block_table[s, 0] * W.BLOCK for s in seqs], np.int64)
+    shape = (len(seqs),) + k.shape[1:]
+    k2 = W.to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * 3)
+    v2 = W.to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    ik2 = W.to_bf16_bits(rng.standard_normal((len(seqs),) + ik.shape[1:]).astype(np.float32) * 3)
+    k, v, ik, slot = (np.concatenate([a, b]) for a, b in ((k, k2), (v, v2), (ik, ik2), (slot, extra)))
+    st = step.DecodeStep(w, g.kv, g.idx, g.block_table)
+    st.run(g.t(k), g.t(v), g.t(ik), g.t(slot), g.q_bf16, g.idx_q_bf16, g.t(w.decode_lens))
+    rs, rl = g.row_lengths()
+    sc = bsp.index_score(g.idx, g.idx_q, w.idx_q_dtype, g.block_table, rs, rl, w.q_len, w.max_pages)
+    gti, gsb, gctx = bsp.topk_select(sc, rs, rl, g.block_table, w.kv_dtype, w.k_pages)
+    out = bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, gsb, gctx, w.k_pages, SM_SCALE)
+    torch.cuda.synchronize()
+    assert st.dev_err.item() == 0
+    assert torch.equal(st.scores, sc)
+    assert torch.equal(st.sparse_bt, gsb) and torch.equal(st.sparse_ctx, gctx)
+    assert torch.equal(st.out, out)
+    # and the oracle, written the same way, agrees on the scores of page 0
+    o = OracleSide(w)
+    O.kv_page_write(w.kv_dtype, w.hkv, o.kv, w.k_scale, w.v_scale, w.idx_dtype, w.hidx, o.idx, k, v, ik, slot)
+    ref, mag = o.scores(want_absdot=True)
+    got = sc.cpu().numpy()
+    for r in range(w.num_rows):
+        if o.row_len[r] > 0:
+            assert abs(got[r, 0] - ref[r, 0]) <= SCORE_REL * mag[r, 0] + 1e-30, r
+
+
 @pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx"])
 def test_decode_step_reuses_another_layers_selection(bsp, name):
     """BSP_REUSE_SELECTION: a second layer's step (its own K/V cache, no
