@@ -67,6 +67,7 @@ def _declare(L):
     L.orc_row_lengths_prefill.argtypes = [vp, vp, i32, i32, vp, vp]
     L.orc_index_score.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, vp, vp, i32, i32, vp, vp, vp, i32]
     L.orc_topk_select.argtypes = [vp, i32, i32, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32]
+    L.orc_topk_select_blocks.argtypes = [vp, i32, i32, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32]
     L.orc_sparse_attention.argtypes = [i32, i32, vp, f32, f32, vp, i32, i32, vp, vp, i32, i32, f32, vp, vp, i32]
     L.orc_dense_attention.argtypes = [i32, i32, vp, f32, f32, vp, i32, i32, vp, i32, vp, vp, i32, f32, vp, vp, i32]
     L.orc_num_threads.restype = i32
@@ -196,6 +197,22 @@ def topk_select(scores, row_seq, row_len, block_table, id_rule, k_pages, force_t
     sub, nsub = _subset(rows)
     lib().orc_topk_select(_p(sc), n, sc.shape[1], _p(rs), _p(rl), _p(bt), bt.shape[1], id_rule, k_pages,
                           1 if force_tail else 0, _p(ti), _p(sb), _p(ctx), _p(sub), nsub)
+    return ti, sb, ctx
+
+
+def topk_select_blocks(scores, row_seq, row_len, block_table, id_rule, k_pages, force_tail=True, rows=None):
+    """128-token blocks as the unit of selection (k_pages // 8 blocks a row)."""
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    rs = np.ascontiguousarray(row_seq, dtype=np.int32)
+    rl = np.ascontiguousarray(row_len, dtype=np.int32)
+    n = sc.shape[0]
+    ti = np.full((n, k_pages), -2, np.int32)
+    sb = np.full((n, k_pages), -2, np.int32)
+    ctx = np.full(n, -2, np.int32)
+    sub, nsub = _subset(rows)
+    lib().orc_topk_select_blocks(_p(sc), n, sc.shape[1], _p(rs), _p(rl), _p(bt), bt.shape[1], id_rule, k_pages,
+                                 1 if force_tail else 0, _p(ti), _p(sb), _p(ctx), _p(sub), nsub)
     return ti, sb, ctx
 
 

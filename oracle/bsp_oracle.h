@@ -24,8 +24,8 @@
  * the fp32 per-token index scale, the fp32 page score).
  *
  * Parity status per routine (see the test-suite for each pin):
- *   codecs, layouts, write, row lengths, index score, top-k and emission,
- *   sparse and dense attention: pinned.
+ *   codecs, layouts, write, row lengths, index score, top-k and emission
+ *   (page- and block-granular), sparse and dense attention: pinned.
  *   The following readings are fixed by this oracle and the GPU path is only
  *   checked for consistency with them ("parity unpinned" in the sense that the
  *   pages print no worked example for them): max-pooling of token scores into
@@ -116,6 +116,14 @@ void orc_topk_select(const float* scores, int rows, int max_pages,
                      const int32_t* block_table, int bt_stride, int id_rule, int k_pages, int force_tail,
                      int32_t* topk_idx, int32_t* sparse_bt, int32_t* sparse_ctx,
                      const int32_t* row_subset, int n_subset);
+
+/* The same with 128-token blocks as the unit of selection: k_pages / 8
+ * blocks per row, each emitting its pages (see topk.c). */
+void orc_topk_select_blocks(const float* scores, int rows, int max_pages,
+                            const int32_t* row_seq, const int32_t* row_len,
+                            const int32_t* block_table, int bt_stride, int id_rule, int k_pages, int force_tail,
+                            int32_t* topk_idx, int32_t* sparse_bt, int32_t* sparse_ctx,
+                            const int32_t* row_subset, int n_subset);
 
 /* ---- step 5: attention ------------------------------------------------- */
 /* q: [tokens, Hkv*G, 128] (bf16 bits or e4m3 bytes); out: bf16 bits, same
