@@ -17,8 +17,10 @@ dependent launch), so no event sits between them in those K steps.  The K
 steps then run once more with an event between kernels, which gives each
 kernel's duration for the roofline (an upper bound: the events serialise the
 kernels).  SM clocks are sampled with nvidia-smi during both passes.  `e2e` repeats the measurement through the public step API with the
-step's inputs copied from pinned host memory and the attention output copied
-back, inside the timed region.  `cpu_baseline` times the CPU oracle (C, OpenMP)
+step's inputs in pinned host memory and the attention output returned to
+pinned host memory, inside the timed region: with copy-engine copies, and (a
+decode step) zero-copy, the kernels loading and storing the pinned buffers
+over NVLink-C2C; the faster is `e2e`, both are listed.  `cpu_baseline` times the CPU oracle (C, OpenMP)
 on a bounded sample of the same workload; `--impl reference` reports that
 oracle as the reference arm.
 
@@ -54,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--select-blocks", action="store_true",
+                    help="128-token blocks as the unit of selection (top_k_pages / 8 blocks a row)")
     return ap.parse_args()
 
 
@@ -165,7 +169,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def workload_desc(w):
+def workload_desc(w, select_blocks=False):
     lens = w.decode_lens
     d = {"workload": w.name, "decode_seqs": int(w.num_decode), "q_len": int(w.q_len),
          "context_min": int(lens.min()) if len(lens) else 0, "context_max": int(lens.max()) if len(lens) else 0,
@@ -176,6 +180,7 @@ def workload_desc(w):
         d["prefill_chunks"] = [list(c) for c in w.prefill_chunks]
         d["pad_rows"] = int(w.num_pad_tokens)
     d["l2"] = "flushed before every step (256 MiB memset, excluded from the step time)"
+    d["selection_unit"] = "128-token block" if select_blocks else "16-token page"
     return d
 
 
@@ -204,9 +209,9 @@ class OracleStep:
     write of their new tokens, e4m3 casts, scores, top-k, attention.  Their
     caches are written once, outside the timing."""
 
-    def __init__(self, w, n):
+    def __init__(self, w, n, blocks=False):
         import oracle as O
-        self.O, self.w = O, w
+        self.O, self.w, self.blocks = O, w, blocks
         seqs = list(range(n))
         self.kv = np.zeros(w.num_blocks * O.kv_block_bytes(w.kv_dtype, w.hkv), np.uint8)
         self.idx = np.zeros(w.num_blocks * w.hidx * O.index_field_bytes(w.idx_dtype), np.uint8)
@@ -233,24 +238,25 @@ class OracleStep:
         iqd = self.iq if w.idx_q_dtype == 0 else O.cast_e4m3(self.iq)
         sc = O.index_score(w.idx_dtype, w.hidx, self.idx, iqd, w.idx_q_dtype, w.block_table, self.rs, self.rl,
                            w.max_pages, rows=self.rows)
-        ti, sb, ctx = O.topk_select(sc, self.rs, self.rl, w.block_table, 1 if w.kv_dtype == 2 else 0, w.k_pages,
-                                    True, rows=self.rows)
+        select = O.topk_select_blocks if self.blocks else O.topk_select
+        ti, sb, ctx = select(sc, self.rs, self.rl, w.block_table, 1 if w.kv_dtype == 2 else 0, w.k_pages, True,
+                             rows=self.rows)
         O.sparse_attention(w.kv_dtype, w.hkv, self.kv, w.k_scale, w.v_scale, qd, w.q_dtype, w.group, sb, ctx,
                            w.sm_scale, rows=self.rows)
         return time.perf_counter() - t0
 
 
-def oracle_sample(w, seconds):
+def oracle_sample(w, seconds, blocks=False):
     """An OracleStep whose run takes about `seconds` (at least one sequence)."""
-    one = OracleStep(w, 1)
+    one = OracleStep(w, 1, blocks)
     t1 = min(one.run() for _ in range(2))
     n = int(max(1, min(w.num_decode, seconds / max(t1, 1e-6))))
-    return one if n == 1 else OracleStep(w, n)
+    return one if n == 1 else OracleStep(w, n, blocks)
 
 
-def cpu_oracle_rate(w, seconds=12.0):
+def cpu_oracle_rate(w, seconds=12.0, blocks=False):
     import oracle as O
-    o = oracle_sample(w, seconds)
+    o = oracle_sample(w, seconds, blocks)
     dt = o.run()
     return o.tokens / dt, O.num_threads(), o.desc + ", one pass"
 
@@ -265,7 +271,7 @@ def run_reference(args):
 
     w = W.workload(args.config)
     # each step a bounded sample of the batch, sized so that the whole run ends within a few minutes
-    o = oracle_sample(w, max(0.005, 120.0 / max(1, args.steps + args.warmup)))
+    o = oracle_sample(w, max(0.005, 120.0 / max(1, args.steps + args.warmup)), args.select_blocks)
     for _ in range(args.warmup):
         o.run()
     times = [o.run() for _ in range(args.steps)]
@@ -274,7 +280,7 @@ def run_reference(args):
     line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": workload_desc(w),
+            "config": workload_desc(w, args.select_blocks),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
                              "sample": o.desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -310,10 +316,11 @@ def run_ours(args):
     k, v, ik, slot = w.step_tokens()
     q, iq = w.queries()
     mixed = bool(w.prefill_chunks)
+    flags = bsp.FORCE_TAIL | (bsp.SELECT_BLOCKS if args.select_blocks else 0)
     if mixed:
-        st = step.MixedStep(w, kv, idx, bt, device=dev)
+        st = step.MixedStep(w, kv, idx, bt, device=dev, flags=flags)
     else:
-        st = step.DecodeStep(w, kv, idx, bt, device=dev)
+        st = step.DecodeStep(w, kv, idx, bt, device=dev, flags=flags)
     inputs = {"k": t(k), "v": t(v), "idx_k": t(ik), "slot": t(slot), "q": t(q), "idx_q": t(iq),
               "seq_lens": t(w.decode_lens)}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -409,37 +416,50 @@ def run_ours(args):
     else:
         roof = dict(kernels[dom], kernel=dom)
 
-    # end to end through the public step API, inputs from pinned host memory
+    # end to end through the public step API, inputs in pinned host memory and
+    # the output returned to pinned host memory, every step.  A decode step
+    # runs it twice: with copy-engine copies (one host-to-device copy of the
+    # packed inputs, one device-to-host copy of the output) and zero-copy (the
+    # step's kernels load the inputs from and store the output to the pinned
+    # buffers over NVLink-C2C).  `e2e` is the faster of the two; both are kept.
     e2e = None
     if not args.no_e2e:
         host = {kk: vv.cpu() for kk, vv in inputs.items()}
-        hs = step.HostDecodeStep(st, host, device=dev)
         Ke = min(K, 500)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
-        for _ in range(3):
-            flush.zero_()
-            hs.run(stream)
-        torch.cuda.synchronize()
-        for i in range(Ke):
-            flush.zero_()
-            ev[i][0].record(stream)
-            hs.run(stream)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), dev)
-        e2e = {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": hs.h2d_bytes, "d2h_bytes_per_step": hs.d2h_bytes}
+
+        def time_host(hs):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+            for _ in range(3):
+                flush.zero_()
+                hs.run(stream)
+            torch.cuda.synchronize()
+            for i in range(Ke):
+                flush.zero_()
+                ev[i][0].record(stream)
+                hs.run(stream)
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), dev)
+            return {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
+                    "h2d_bytes_per_step": hs.h2d_bytes, "d2h_bytes_per_step": hs.d2h_bytes}
+
+        modes = {"copy_engine": step.HostDecodeStep(st, host, device=dev)}
+        if not mixed:
+            modes["zero_copy"] = step.HostDecodeStep(st, host, device=dev, zero_copy=True)
+        res = {m: time_host(hs) for m, hs in modes.items()}
+        best = max(res, key=lambda m: res[m]["value"])
+        e2e = dict(res[best], transfer=best, modes=res)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, threads, desc = cpu_oracle_rate(w)
+        r, threads, desc = cpu_oracle_rate(w, blocks=args.select_blocks)
         cpu = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
 
     if rank == 0:
         line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "e4m3" if w.kv_dtype == 1 else ("mxfp4" if w.kv_dtype == 2 else "bf16"),
-                "data": "synthetic", "config": workload_desc(w), "roofline": roof, "kernels": kernels,
+                "data": "synthetic", "config": workload_desc(w, args.select_blocks), "roofline": roof, "kernels": kernels,
                 "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
                 "device_errors": err}
         print(json.dumps(line))

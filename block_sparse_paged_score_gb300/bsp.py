@@ -16,6 +16,7 @@ from . import build as _build
 BF16, FP8_E4M3, MXFP4 = 0, 1, 2
 FORCE_TAIL = 1
 REUSE_SELECTION = 2  # decode step: attend with another layer's sparse_bt / sparse_ctx
+SELECT_BLOCKS = 4  # top-k: 128-token blocks are the unit of selection
 DEVERR = {1: "page id", 2: "block id", 4: "group sequence", 8: "timeout", 16: "slot"}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error"}
 

@@ -276,6 +276,7 @@ static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_p
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1 || k_pages < 1 || !valid_dtype(kv_dtype))
     return BSP_ERR_INVALID_ARG;
   if (k_pages > 2048 || max_pages > 65536) return BSP_ERR_UNSUPPORTED;
+  if ((flags & BSP_SELECT_BLOCKS) && k_pages < kPagesPerSide) return BSP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_pages) > static_cast<int64_t>(bt_stride) * 8) return BSP_ERR_INVALID_ARG;
   if (num_rows == 0) return BSP_OK;
   if (!scores || !row_seq || !row_len || !block_table || !topk_idx || !sparse_bt || !sparse_ctx || !al(scores, 16))
@@ -295,6 +296,7 @@ static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_p
   p.sparse_bt = sparse_bt;
   p.sparse_ctx = sparse_ctx;
   p.rows_per_seq = rows_per_seq;
+  p.blocks = (flags & BSP_SELECT_BLOCKS) ? 1 : 0;
   bsp_status st = cuda_status(launch_topk_select(p, reinterpret_cast<cudaStream_t>(stream)));
   if (st == BSP_OK) ++g_launches;
   return st;
@@ -475,7 +477,8 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
     return st;
   mark(2);
   if (!reuse && (st = topk_impl(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
-                                a->kv->dtype, a->k_pages, a->flags & BSP_FORCE_TAIL, a->topk_idx, a->sparse_bt,
+                                a->kv->dtype, a->k_pages, a->flags & (BSP_FORCE_TAIL | BSP_SELECT_BLOCKS),
+                                a->topk_idx, a->sparse_bt,
                                 a->sparse_ctx, stream, a->q_len * hkv)) != BSP_OK)
     return st;
   mark(3);

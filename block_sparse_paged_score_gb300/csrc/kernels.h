@@ -106,6 +106,7 @@ struct TopkParams {
   int32_t bt_stride, id_mul;  // id = block * id_mul + p % 8
   int32_t k_pages, force_tail;
   int32_t rows_per_seq;  // > 0: row r belongs to sequence r / rows_per_seq (no row_seq lookup first)
+  int32_t blocks;        // 1: select 128-token blocks (k_pages / 8 of them), each emitting its pages
   int32_t* topk_idx;
   int32_t* sparse_bt;
   int32_t* sparse_ctx;

@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
       uint16_t* dst = static_cast<uint16_t*>(p.out) + (token * hq + static_cast<int64_t>(h) * p.group + head) * kDim + d;
       *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(O.x * f, O.y * f), pack_bf16x2(O.z * f, O.w * f));
     }
-    cluster_sync();  // peers are done reading this CTA's shared memory
+    cluster_sync_relaxed();  // peers are done reading this CTA's shared memory
     return;
   }
 

@@ -308,6 +308,79 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
 #define BSP_TOPK_WARP_MAX 128
 #endif
 
+// Radix select over keys held in registers by a CTA: thread t holds NK keys
+// of candidates first..first+NK-1 (valid below n_cand).  Four 8-bit passes,
+// most significant digit first, each with one shared-memory histogram (the
+// four are zeroed by the caller before its first __syncthreads) and one warp
+// scanning its 256 bins from the top, find tau, the need-th largest key, and
+// take_eq, how many keys equal to tau are taken.  Block-wide: every thread
+// of the CTA calls it.
+template <int NK>
+__device__ __forceinline__ void radix_select_regs(const uint32_t (&key)[NK], int first, int n_cand, int need,
+                                                  int (&s_hist)[4][256], uint32_t& s_digit, int& s_above, int warp,
+                                                  int lane, uint32_t& tau, int& take_eq) {
+  uint32_t prefix = 0, mask = 0;
+  int krem = need;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    __syncthreads();  // histograms zeroed; the previous pass's digit read
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+      if (first + j < n_cand && (key[j] & mask) == prefix) atomicAdd(&s_hist[pass][(key[j] >> shift) & 255], 1);
+    __syncthreads();
+    if (warp == 0) {
+      // lane owns bins 255-8*lane .. 248-8*lane (descending); find the digit
+      // where the running count from the top first reaches krem
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = s_hist[pass][255 - 8 * lane - j];
+        sum += c[j];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - sum;  // keys in higher bins
+      if (run < krem && krem <= incl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < krem && krem <= run + c[j]) {
+            s_digit = static_cast<uint32_t>(255 - 8 * lane - j);
+            s_above = run;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    krem -= s_above;
+    prefix |= s_digit << shift;
+    mask |= 255u << shift;
+  }
+  tau = prefix;
+  take_eq = krem;
+}
+
+// exclusive prefix over the CTA (in thread order) of a per-thread count
+// packed as (gt << 16) | eq; both fields stay below 2^16
+__device__ __forceinline__ int cta_exclusive_packed(int packed, int* s_warp, int warp, int lane) {
+  int x = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int before = x - packed;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  return before;
+}
+
 // One CTA of 256 threads per row of up to 256*KPT pages.  Thread t owns the
 // KPT consecutive pages t*KPT.. in registers (and the ids of the one or two
 // 128-token blocks they lie in, loaded up front).  A radix select of four
@@ -374,52 +447,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
 
   uint32_t tau = 0;
   int take_eq = 0;
-  if (radix) {
-    uint32_t prefix = 0, mask = 0;
-    int krem = need;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      __syncthreads();  // histograms zeroed; the previous pass's digit read
-#pragma unroll
-      for (int j = 0; j < KPT; ++j)
-        if (first + j < n_cand && (key[j] & mask) == prefix) atomicAdd(&s_hist[pass][(key[j] >> shift) & 255], 1);
-      __syncthreads();
-      if (warp == 0) {
-        // lane owns bins 255-8*lane .. 248-8*lane (descending); find the digit
-        // where the running count from the top first reaches krem
-        int c[8], sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = s_hist[pass][255 - 8 * lane - j];
-          sum += c[j];
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        int run = incl - sum;  // keys in higher bins
-        if (run < krem && krem <= incl) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (run < krem && krem <= run + c[j]) {
-              s_digit = static_cast<uint32_t>(255 - 8 * lane - j);
-              s_above = run;
-            }
-            run += c[j];
-          }
-        }
-      }
-      __syncthreads();
-      krem -= s_above;
-      prefix |= s_digit << shift;
-      mask |= 255u << shift;
-    }
-    tau = prefix;
-    take_eq = krem;
-  }
+  if (radix) radix_select_regs<KPT>(key, first, n_cand, need, s_hist, s_digit, s_above, warp, lane, tau, take_eq);
 
   // (keys > tau, keys == tau) of this thread, scanned over the block in page order
   int gt = 0, eq = 0;
@@ -429,17 +457,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
     gt += valid && (all || (radix && key[j] > tau));
     eq += valid && radix && key[j] == tau;
   }
-  const int packed = (gt << 16) | eq;  // both < 2^16
-  int x = packed;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  int before = x - packed;
-  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  const int before = cta_exclusive_packed((gt << 16) | eq, s_warp, warp, lane);
   int eqr = before & 0xFFFF;
   int pos = (before >> 16) + min(eqr, take_eq);
   bool tail_sel = false;
@@ -476,6 +494,138 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   }
 }
 
+// 128-token blocks as the unit of selection (pages_per_block = 8).  One CTA
+// of 256 threads per row; thread t owns blocks t*BPT.. with their ids in
+// registers.  A block's key is the order key of the largest page score among
+// its pages below n.  The same radix select and block scan as the
+// page-granular CTA kernel find the selected blocks and their ranks; the
+// block of rank j emits its pages (all 8, or the row's last n - 8*(nb-1)) at
+// table positions 8j.., so the pages come out ascending.  With force_tail the
+// tail block nb-1 is always selected and takes the last rank.
+template <int BPT>
+__global__ void __launch_bounds__(kCtaThreads) topk_block_kernel(TopkParams p) {
+  __shared__ int s_hist[4][256];
+  __shared__ int s_warp[kCtaThreads / 32];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_above;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
+  const bool in_step = p.rows_per_seq > 0;  // as in the page-granular kernel
+  if (!in_step) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  const int max_len = p.max_pages * kPage;
+  const int L = min(max(p.row_len[r], 0), max_len);
+  const int n = (L + kPage - 1) / kPage;
+  const int nb = (n + kPagesPerSide - 1) / kPagesPerSide;
+  const int kb = min(p.k_pages / kPagesPerSide, nb);
+  int32_t* ti = p.topk_idx + static_cast<int64_t>(r) * p.k_pages;
+  int32_t* bt = p.sparse_bt + static_cast<int64_t>(r) * p.k_pages;
+  for (int m = tid; m < p.k_pages; m += kCtaThreads) ti[m] = bt[m] = -1;  // emitted entries overwrite these
+  if (kb == 0) {
+    if (tid == 0) p.sparse_ctx[r] = 0;
+    if (in_step) pdl_wait();
+    return;
+  }
+  const int n_cand = p.force_tail ? nb - 1 : nb;
+  const int need = p.force_tail ? kb - 1 : kb;
+  const bool all = need >= n_cand, none = need == 0, radix = !all && !none;
+
+  const int first = tid * BPT;
+  const int64_t bt_row = static_cast<int64_t>(p.rows_per_seq > 0 ? r / p.rows_per_seq : p.row_seq[r]) * p.bt_stride;
+  int32_t ids[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) ids[j] = first + j < nb ? p.block_table[bt_row + first + j] * p.id_mul : 0;
+  if (in_step) {
+    pdl_wait();  // the scores
+    pdl_trigger();
+  }
+  const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
+  // rows of a multiple of 8 pages: a block's 8 scores are two aligned float4
+  // (the score buffer is 16-byte aligned), masked to the pages below n
+  const bool vec = (p.max_pages & 7) == 0;
+  uint32_t key[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    key[j] = 0u;
+    const int b = first + j;
+    if (radix && b < n_cand) {
+      const int p0 = b * kPagesPerSide, np = min(kPagesPerSide, n - p0);
+      float best;
+      if (vec) {
+        const float4 x = reinterpret_cast<const float4*>(srow + p0)[0];
+        const float4 y = reinterpret_cast<const float4*>(srow + p0)[1];
+        const float v[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+        best = v[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) best = k < np ? fmaxf(best, v[k]) : best;
+      } else {
+        best = srow[p0];
+        for (int pg = p0 + 1; pg < p0 + np; ++pg) best = fmaxf(best, srow[pg]);
+      }
+      key[j] = order_key(best);
+    }
+  }
+
+  uint32_t tau = 0;
+  int take_eq = 0;
+  if (radix) radix_select_regs<BPT>(key, first, n_cand, need, s_hist, s_digit, s_above, warp, lane, tau, take_eq);
+
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const bool valid = first + j < n_cand;
+    gt += valid && (all || (radix && key[j] > tau));
+    eq += valid && radix && key[j] == tau;
+  }
+  const int before = cta_exclusive_packed((gt << 16) | eq, s_warp, warp, lane);
+  int eqr = before & 0xFFFF;
+  int rank = (before >> 16) + min(eqr, take_eq);
+  bool tail_sel = false;
+  const int tail_pages = n - kPagesPerSide * (nb - 1);  // pages of the row's last block
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const int b = first + j;
+    const bool valid = b < n_cand;
+    const bool is_eq = valid && radix && key[j] == tau;
+    const bool sel = valid && !none && (all || (radix && key[j] > tau) || (is_eq && eqr < take_eq));
+    eqr += is_eq;
+    if (sel && rank < need) {
+      const int np = b == nb - 1 ? tail_pages : kPagesPerSide;
+      for (int k = 0; k < np; ++k) {
+        ti[kPagesPerSide * rank + k] = kPagesPerSide * b + k;
+        bt[kPagesPerSide * rank + k] = ids[j] + k;
+      }
+      ++rank;
+    }
+    if (b == nb - 1) tail_sel = sel;
+  }
+  // the owner of block nb-1 finishes the row: the forced tail block, and the
+  // context length (the tail block, if selected, holds the last entries)
+  const int tail_len = L - kPage * (n - 1);
+  if (first <= nb - 1 && nb - 1 < first + BPT) {
+    int32_t id = ids[0];
+#pragma unroll
+    for (int j = 1; j < BPT; ++j)
+      if (nb - 1 - first == j) id = ids[j];
+    if (p.force_tail)
+      for (int k = 0; k < tail_pages; ++k) {
+        ti[kPagesPerSide * (kb - 1) + k] = kPagesPerSide * (nb - 1) + k;
+        bt[kPagesPerSide * (kb - 1) + k] = id + k;
+      }
+    p.sparse_ctx[r] = (p.force_tail || tail_sel)
+                          ? kPage * (kPagesPerSide * (kb - 1) + tail_pages - 1) + tail_len
+                          : kPage * kPagesPerSide * kb;
+  }
+}
+
+template <int BPT>
+cudaError_t launch_blocks(const TopkParams& p, cudaStream_t s) {
+  const cudaError_t e = launch_kernel(topk_block_kernel<BPT>, dim3(p.num_rows), dim3(kCtaThreads), 0, s, 0, p);
+  return e != cudaSuccess ? e : cudaPeekAtLastError();
+}
+
 template <int KPT>
 cudaError_t launch_cta(const TopkParams& p, cudaStream_t s) {
   const cudaError_t e = launch_kernel(topk_cta_kernel<KPT>, dim3(p.num_rows), dim3(kCtaThreads), 0, s, 0, p);
@@ -492,6 +642,15 @@ cudaError_t launch_warp(const TopkParams& p, cudaStream_t s) {
 
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.num_rows == 0) return cudaSuccess;
+  if (p.blocks) {
+    const int nblk = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+    if (nblk <= 1 * kCtaThreads) return launch_blocks<1>(p, s);
+    if (nblk <= 2 * kCtaThreads) return launch_blocks<2>(p, s);
+    if (nblk <= 4 * kCtaThreads) return launch_blocks<4>(p, s);
+    if (nblk <= 8 * kCtaThreads) return launch_blocks<8>(p, s);
+    if (nblk <= 16 * kCtaThreads) return launch_blocks<16>(p, s);
+    return launch_blocks<32>(p, s);  // max_pages <= 65536
+  }
   if (p.max_pages <= 128 && BSP_TOPK_WARP_MAX >= 128) return launch_warp<4>(p, s);
   if (p.max_pages <= 512 && BSP_TOPK_WARP_MAX >= 512) return launch_warp<16>(p, s);
   if (p.max_pages <= 1024 && BSP_TOPK_WARP_MAX >= 1024) return launch_warp<32>(p, s);

@@ -19,7 +19,7 @@ from . import bsp
 
 
 class DecodeStep:
-    def __init__(self, w, kv, idx, block_table, device="cuda"):
+    def __init__(self, w, kv, idx, block_table, device="cuda", flags=bsp.FORCE_TAIL):
         self.w = w
         self.kv, self.idx = kv, idx
         self.block_table = block_table
@@ -43,7 +43,7 @@ class DecodeStep:
         a.num_q_heads = w.hq
         a.num_seqs, a.q_len = w.num_decode, w.q_len
         a.block_table, a.bt_stride = block_table.data_ptr(), block_table.shape[1]
-        a.max_pages, a.k_pages, a.flags, a.sm_scale = w.max_pages, w.k_pages, bsp.FORCE_TAIL, w.sm_scale
+        a.max_pages, a.k_pages, a.flags, a.sm_scale = w.max_pages, w.k_pages, flags, w.sm_scale
         a.row_seq, a.row_len, a.scores = self.row_seq.data_ptr(), self.row_len.data_ptr(), self.scores.data_ptr()
         a.topk_idx, a.sparse_bt, a.sparse_ctx = (self.topk_idx.data_ptr(), self.sparse_bt.data_ptr(),
                                                  self.sparse_ctx.data_ptr())
@@ -65,11 +65,19 @@ class HostDecodeStep:
     """End-to-end step: pinned host inputs -> device -> step -> host output.
 
     The step's inputs sit back to back (256-byte aligned) in one pinned host
-    buffer, so a step makes one host-to-device copy of all of them and one
-    device-to-host copy of the attention output."""
+    buffer.  With zero_copy=False a step makes one host-to-device copy of all
+    of them and one device-to-host copy of the attention output.  With
+    zero_copy=True (a DecodeStep only) no copy is issued: the step's kernels
+    read their inputs straight from the pinned buffer and the attention writes
+    its output straight into pinned host memory -- pinned memory is mapped
+    into the device's address space, and on a Grace-Blackwell node these
+    loads and stores cross the NVLink-C2C link."""
 
-    def __init__(self, step, host_inputs, device="cuda"):
+    def __init__(self, step, host_inputs, device="cuda", zero_copy=False):
         self.step = step
+        self.zero_copy = zero_copy
+        if zero_copy and not isinstance(step, DecodeStep):
+            raise ValueError("zero_copy needs a DecodeStep")
         offs, total = {}, 0
         for k, v in host_inputs.items():
             offs[k] = total
@@ -83,6 +91,10 @@ class HostDecodeStep:
             self.host_buf[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
             self.dev[k] = self.dev_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
         self.out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        self.host = {}
+        for k, v in host_inputs.items():
+            n = v.numel() * v.element_size()
+            self.host[k] = self.host_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
 
     @property
     def h2d_bytes(self):
@@ -94,6 +106,15 @@ class HostDecodeStep:
 
     def run(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
+        if self.zero_copy:
+            h, a = self.host, self.step.args
+            dev_out = a.out
+            a.out = self.out_host.data_ptr()
+            try:
+                self.step.run(h["k"], h["v"], h["idx_k"], h["slot"], h["q"], h["idx_q"], h["seq_lens"], stream=s)
+            finally:
+                a.out = dev_out
+            return self.out_host
         with torch.cuda.stream(s):
             self.dev_buf.copy_(self.host_buf, non_blocking=True)
             d = self.dev
@@ -109,8 +130,9 @@ class MixedStep:
     scorer and attend plan-free.  Same run() signature as DecodeStep; `events`
     (5 torch events) mark the same phases."""
 
-    def __init__(self, w, kv, idx, block_table, device="cuda"):
+    def __init__(self, w, kv, idx, block_table, device="cuda", flags=bsp.FORCE_TAIL):
         self.w, self.kv, self.idx, self.block_table = w, kv, idx, block_table
+        self.flags = flags
         T, rows = w.num_tokens, w.num_rows
         self.nd_tok, self.nd = w.num_decode_tokens, w.num_decode_rows
         e = lambda *s, dt=torch.int32: torch.empty(s, dtype=dt, device=device)  # noqa: E731
@@ -149,7 +171,7 @@ class MixedStep:
                                 self.scores[nd:], self.dev_err, s)
         mark(2)
         bsp.topk_select(self.scores, self.row_seq, self.row_len, self.block_table, w.kv_dtype, w.k_pages,
-                        bsp.FORCE_TAIL, self.topk_idx, self.sparse_bt, self.sparse_ctx, s)
+                        self.flags, self.topk_idx, self.sparse_bt, self.sparse_ctx, s)
         mark(3)
         if nd:
             bsp.sparse_pa_decode(self.kv, q[:ndt], w.q_dtype, w.hq, self.sparse_bt[:nd], self.sparse_ctx[:nd],

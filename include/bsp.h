@@ -86,6 +86,8 @@ typedef enum {
 #define BSP_FORCE_TAIL 1 /* the tail page of every row is always selected */
 /* decode-step flag: reuse another layer's selection (see bsp_sparse_decode_step) */
 #define BSP_REUSE_SELECTION 2
+/* top-k flag: 128-token blocks are the unit of selection (see bsp_topk_select) */
+#define BSP_SELECT_BLOCKS 4
 
 /* ------------------------------------------------------------------------
  * K/V cache descriptor.
@@ -249,6 +251,14 @@ bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q
  *             kv_dtype MXFP4 (128-token fields): block_table[s][p/8]*8 + p%8
  *   sparse_ctx int32 [rows]: 16*(selected full pages) + (valid tokens of the
  *             tail page if selected); 0 for L_r = 0.
+ * With BSP_SELECT_BLOCKS the unit of selection is the 128-token block
+ * ([ATOM-2962] commit "... page-128 block table": one score per 128 tokens,
+ * an emit with pages_per_block): a block's score is the largest score of its
+ * pages below n; kb' = min(k_pages/8, ceil(n/8)) blocks are selected (with
+ * BSP_FORCE_TAIL the tail block always, the rest by score, equal scores to
+ * the lower block), and each selected block, ascending, emits its pages below
+ * n with the page ids above -- at most 8*kb' entries, -1 padded, sparse_ctx as
+ * above.  Needs k_pages >= 8 (else BSP_ERR_INVALID_ARG).
  * k_pages <= 2048, max_pages <= 65536.
  * ---------------------------------------------------------------------- */
 bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pages,
@@ -330,7 +340,11 @@ bsp_status bsp_sparse_pa_prefill(const bsp_kv_cache* kv, const void* q, int32_t 
 /* ------------------------------------------------------------------------
  * The whole decode step as one call: write the step's new tokens, cast the
  * queries the writer emits as e4m3, compute the row lengths, score, select
- * and attend.  All pointers are device pointers; buffers are caller-owned.
+ * and attend.  Buffers are caller-owned.  Pointers are device pointers; the
+ * step's inputs (k_new, v_new, idx_k_new, slot, q, idx_q, seq_lens) and `out`
+ * may instead point into pinned host memory (cudaHostAlloc / page-locked,
+ * which unified addressing maps into the device's address space): the
+ * kernels then load and store them in place, with no copy.
  * `events` (nullable) receives 5 cudaEventRecord calls on `stream`: before
  * the write, before scoring, before the selection, before the attention, and
  * at the end.
@@ -367,7 +381,7 @@ typedef struct bsp_decode_step_args {
   int32_t bt_stride;
   int32_t max_pages;
   int32_t k_pages;
-  int32_t flags;              /* BSP_FORCE_TAIL, BSP_REUSE_SELECTION */
+  int32_t flags;              /* BSP_FORCE_TAIL, BSP_REUSE_SELECTION, BSP_SELECT_BLOCKS */
   float sm_scale;
   /* outputs and scratch (caller-owned device memory) */
   int32_t* row_seq;           /* [rows] */

@@ -411,3 +411,25 @@ def test_host_argument_errors(bsp):
         bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb128).cuda(), torch.from_numpy(ctx).cuda(),
                              128, ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx"])
+def test_host_step_zero_copy_matches_device_step(bsp, name):
+    """The decode step fed straight from pinned host memory (its kernels load
+    the inputs and store the output in place) equals the step on device
+    copies, bit for bit, and so does the copy-engine host step."""
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides(name)
+    st = step.DecodeStep(w, g.kv, g.idx, g.block_table)
+    k, v, ik, slot = w.step_tokens()
+    dev = {"k": g.t(k), "v": g.t(v), "idx_k": g.t(ik), "slot": g.t(slot), "q": g.q_bf16, "idx_q": g.idx_q_bf16,
+           "seq_lens": g.t(w.decode_lens)}
+    st.run(dev["k"], dev["v"], dev["idx_k"], dev["slot"], dev["q"], dev["idx_q"], dev["seq_lens"])
+    ref = st.out.clone()
+    host = {kk: vv.cpu() for kk, vv in dev.items()}
+    for zc in (True, False):
+        hs = step.HostDecodeStep(st, host, zero_copy=zc)
+        out = hs.run()
+        torch.cuda.synchronize()
+        assert st.dev_err.item() == 0
+        assert torch.equal(out, ref.cpu()), zc
