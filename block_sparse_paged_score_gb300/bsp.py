@@ -49,7 +49,7 @@ class DecodeStepArgs(C.Structure):
                 ("k_pages", C.c_int32), ("flags", C.c_int32), ("sm_scale", C.c_float),
                 ("row_seq", C.c_void_p), ("row_len", C.c_void_p), ("scores", C.c_void_p), ("topk_idx", C.c_void_p),
                 ("sparse_bt", C.c_void_p), ("sparse_ctx", C.c_void_p), ("out", C.c_void_p), ("ws", C.c_void_p),
-                ("ws_bytes", C.c_size_t), ("dev_err", C.c_void_p)]
+                ("ws_bytes", C.c_size_t), ("dev_err", C.c_void_p), ("sel_counters", C.c_void_p)]
 
 
 _lib = None

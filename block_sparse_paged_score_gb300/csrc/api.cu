@@ -189,7 +189,8 @@ bsp_status bsp_row_lengths_prefill(const int32_t* query_req_id, const int32_t* q
 static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
                                    const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
                                    const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
-                                   float* scores, int32_t* dev_err, bsp_stream_t stream, int32_t seq_is_group) {
+                                   float* scores, int32_t* dev_err, bsp_stream_t stream, int32_t seq_is_group,
+                                   const TopkParams* sel = nullptr, int32_t* sel_counters = nullptr) {
   bsp_status st = check_idx(idx);
   if (st != BSP_OK) return st;
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1) return BSP_ERR_INVALID_ARG;
@@ -218,6 +219,10 @@ static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q
   p.scores = scores;
   p.err = dev_err;
   p.seq_is_group = seq_is_group;
+  if (sel) {
+    p.sel = *sel;
+    p.sel_counters = sel_counters;
+  }
   st = cuda_status(launch_index_score(p, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
   if (st == BSP_OK) ++g_launches;
   return st;
@@ -268,20 +273,21 @@ bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q
   return st;
 }
 
-// rows_per_seq > 0: row r belongs to sequence r / rows_per_seq (the decode step's own rows)
-static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
-                            const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
-                            int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt,
-                            int32_t* sparse_ctx, bsp_stream_t stream, int32_t rows_per_seq) {
+// The selector's parameters, checked.  rows_per_seq > 0: row r belongs to
+// sequence r / rows_per_seq (the decode step's own rows).
+static bsp_status topk_params(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
+                              const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
+                              int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt,
+                              int32_t* sparse_ctx, int32_t rows_per_seq, TopkParams& p) {
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1 || k_pages < 1 || !valid_dtype(kv_dtype))
     return BSP_ERR_INVALID_ARG;
   if (k_pages > 2048 || max_pages > 65536) return BSP_ERR_UNSUPPORTED;
   if ((flags & BSP_SELECT_BLOCKS) && k_pages < kPagesPerSide) return BSP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_pages) > static_cast<int64_t>(bt_stride) * 8) return BSP_ERR_INVALID_ARG;
-  if (num_rows == 0) return BSP_OK;
-  if (!scores || !row_seq || !row_len || !block_table || !topk_idx || !sparse_bt || !sparse_ctx || !al(scores, 16))
+  if (num_rows > 0 &&
+      (!scores || !row_seq || !row_len || !block_table || !topk_idx || !sparse_bt || !sparse_ctx || !al(scores, 16)))
     return BSP_ERR_INVALID_ARG;
-  TopkParams p{};
+  p = TopkParams{};
   p.scores = scores;
   p.num_rows = num_rows;
   p.max_pages = max_pages;
@@ -297,7 +303,18 @@ static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_p
   p.sparse_ctx = sparse_ctx;
   p.rows_per_seq = rows_per_seq;
   p.blocks = (flags & BSP_SELECT_BLOCKS) ? 1 : 0;
-  bsp_status st = cuda_status(launch_topk_select(p, reinterpret_cast<cudaStream_t>(stream)));
+  return BSP_OK;
+}
+
+static bsp_status topk_impl(const float* scores, int32_t num_rows, int32_t max_pages, const int32_t* row_seq,
+                            const int32_t* row_len, const int32_t* block_table, int32_t bt_stride, int32_t kv_dtype,
+                            int32_t k_pages, int32_t flags, int32_t* topk_idx, int32_t* sparse_bt,
+                            int32_t* sparse_ctx, bsp_stream_t stream, int32_t rows_per_seq) {
+  TopkParams p;
+  bsp_status st = topk_params(scores, num_rows, max_pages, row_seq, row_len, block_table, bt_stride, kv_dtype, k_pages,
+                              flags, topk_idx, sparse_bt, sparse_ctx, rows_per_seq, p);
+  if (st != BSP_OK || num_rows == 0) return st;
+  st = cuda_status(launch_topk_select(p, reinterpret_cast<cudaStream_t>(stream)));
   if (st == BSP_OK) ++g_launches;
   return st;
 }
@@ -470,16 +487,30 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   mark(1);
   // the step's rows are decode-ordered (row_seq = token / q_len, as the prep
   // kernel writes it): the scorer and the selector find a row's sequence
-  // without reading row_seq first
+  // without reading row_seq first.  With sel_counters the scorer's last CTA
+  // of each query group selects the group's rows (no selector launch).
+  const int32_t topk_flags = a->flags & (BSP_FORCE_TAIL | BSP_SELECT_BLOCKS);
+  const bool fused = !reuse && a->sel_counters &&
+                     index_score_can_select(a->idx->dtype, a->idx_q_dtype, a->max_pages,
+                                            (a->flags & BSP_SELECT_BLOCKS) != 0);
+  TopkParams sel;
+  if (fused) {
+    if (!al(a->sel_counters, 4)) return BSP_ERR_INVALID_ARG;
+    if ((st = topk_params(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
+                          a->kv->dtype, a->k_pages, topk_flags, a->topk_idx, a->sparse_bt, a->sparse_ctx,
+                          a->q_len * hkv, sel)) != BSP_OK)
+      return st;
+  }
   if (!reuse &&
       (st = index_score_impl(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
-                             a->q_len, a->max_pages, a->scores, a->dev_err, stream, 1)) != BSP_OK)
+                             a->q_len, a->max_pages, a->scores, a->dev_err, stream, 1, fused ? &sel : nullptr,
+                             fused ? a->sel_counters : nullptr)) != BSP_OK)
     return st;
   mark(2);
-  if (!reuse && (st = topk_impl(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
-                                a->kv->dtype, a->k_pages, a->flags & (BSP_FORCE_TAIL | BSP_SELECT_BLOCKS),
-                                a->topk_idx, a->sparse_bt,
-                                a->sparse_ctx, stream, a->q_len * hkv)) != BSP_OK)
+  if (!reuse && !fused &&
+      (st = topk_impl(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
+                      a->kv->dtype, a->k_pages, topk_flags, a->topk_idx, a->sparse_bt, a->sparse_ctx, stream,
+                      a->q_len * hkv)) != BSP_OK)
     return st;
   mark(3);
   // the attention's queries were written two launches back (or are the
@@ -510,6 +541,6 @@ const char* bsp_status_str(bsp_status s) {
 
 int32_t bsp_last_cuda_error(void) { return g_last_cuda_error.load(); }
 int64_t bsp_launch_count(void) { return g_launches.load(); }
-int32_t bsp_version(void) { return 100; }
+int32_t bsp_version(void) { return 110; }
 
 }  // extern "C"

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_row.cuh"
 
 namespace bsp {
 
@@ -86,7 +87,34 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off,
   }
 }
 
-template <int KEY>
+// The selection tail of the decode step's scorer: every CTA of a (query
+// group, index head) unit has written its chunk's scores; the last one to
+// finish -- an arrival count per unit -- reads the unit's score rows back
+// through L2 and selects each row (select_row_cta with 128 threads, SEL
+// pages a thread), then zeroes the count for the next step.  The ring is
+// idle by then and holds the histograms.
+template <int SEL>
+__device__ __forceinline__ void select_unit(const IndexScoreParams& p, const int* s_row, int ntok, uint8_t* smem) {
+  __shared__ int s_last;
+  __threadfence();  // this thread's score stores, before the count
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&p.sel_counters[blockIdx.x], 1) == static_cast<int>(gridDim.y) - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // the other CTAs' scores, after the count
+  auto& hist = *reinterpret_cast<int(*)[4][256]>(smem);
+  int* s_warp = reinterpret_cast<int*>(smem + 4096);
+  uint32_t& s_digit = *reinterpret_cast<uint32_t*>(smem + 4096 + 16);
+  int& s_above = *reinterpret_cast<int*>(smem + 4096 + 20);
+  for (int j = 0; j < ntok; ++j) {
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&hist[0][0])[i] = 0;
+    select_row_cta<SEL, 128>(p.sel, s_row[j], hist, s_warp, s_digit, s_above, false);
+    __syncthreads();  // the next row reuses the histograms and the scan slots
+  }
+  if (threadIdx.x == 0) p.sel_counters[blockIdx.x] = 0;
+}
+
+template <int KEY, int SEL>
 __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   constexpr int FB = KeyFmt<KEY>::kField;
   const int S = p.stages;  // ring depth, 1..kStages
@@ -141,7 +169,7 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
     for (int i = tid; i < ntok * npg; i += blockDim.x)
       p.scores[static_cast<int64_t>(s_row[i / npg]) * p.max_pages + pfirst + i % npg] = -INFINITY;
   }
-  if (nb == 0) return;
+  if (nb > 0) {
   if (tid < nb) {
     int bid = p.seq_is_group ? bid_early : p.block_table[static_cast<int64_t>(seq) * p.bt_stride + blk0 + tid];
     if (bid < 0 || bid >= p.num_blocks) {
@@ -297,14 +325,16 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
       issue(i + S);
     }
   }
+  }  // nb > 0
+  if constexpr (SEL > 0) select_unit<SEL>(p, s_row, ntok, smem);
 }
 
 // the dynamic shared-memory opt-in (once per process; per function)
-template <int KEY>
+template <int KEY, int SEL>
 cudaError_t configure_key() {
   static bool configured = false;
   if (configured) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY, SEL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_bytes<KEY>(KeyFmt<KEY>::kStages));
   if (e == cudaSuccess) configured = true;
   return e;
@@ -312,14 +342,15 @@ cudaError_t configure_key() {
 
 // resident CTAs per SM with a ring of `stages` fields (queried once per depth;
 // a failed query assumes 1)
-template <int KEY>
+template <int KEY, int SEL>
 int occupancy_key(int stages) {
   static int cache[KeyFmt<KEY>::kStages + 1] = {};
   if (!cache[stages]) {
     int n = 0;
-    cudaError_t e = configure_key<KEY>();
+    cudaError_t e = configure_key<KEY, SEL>();
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<KEY>, 128, smem_bytes<KEY>(stages));
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<KEY, SEL>, 128,
+                                                        smem_bytes<KEY>(stages));
     cache[stages] = (e == cudaSuccess && n > 0) ? n : 1;
   }
   return cache[stages];
@@ -337,14 +368,14 @@ int occupancy_key(int stages) {
 // retire at once.
 constexpr double kStartBytes = 1.5 * kFp8IndexField;
 
-template <int KEY>
+template <int KEY, int SEL>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
   const double start_blocks = kStartBytes / KeyFmt<KEY>::kField;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {
     const int stages = std::min(cb, KeyFmt<KEY>::kStages);
-    const int64_t resident = static_cast<int64_t>(occupancy_key<KEY>(stages)) * num_sms;
+    const int64_t resident = static_cast<int64_t>(occupancy_key<KEY, SEL>(stages)) * num_sms;
     const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
     const int64_t waves = (ctas + resident - 1) / resident;
     const double cost = static_cast<double>(waves) * (cb + start_blocks);
@@ -357,42 +388,57 @@ void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   }
 }
 
-template <int KEY>
-cudaError_t launch_key(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {
-  const cudaError_t c = configure_key<KEY>();
+template <int KEY, int SEL>
+cudaError_t launch_key(IndexScoreParams p, int64_t max_blocks, int num_sms, cudaStream_t s) {
+  plan_key<KEY, SEL>(p, max_blocks, num_sms);
+  const cudaError_t c = configure_key<KEY, SEL>();
   if (c != cudaSuccess) return c;
-  const cudaError_t e = launch_kernel(index_score_kernel<KEY>, grid, dim3(128), smem_bytes<KEY>(p.stages), s, 0, p);
+  const int64_t cb = p.blocks_per_chunk;
+  const dim3 grid(static_cast<unsigned>(p.num_groups * p.hidx), static_cast<unsigned>((max_blocks + cb - 1) / cb));
+  const cudaError_t e =
+      launch_kernel(index_score_kernel<KEY, SEL>, grid, dim3(128), smem_bytes<KEY>(p.stages), s, 0, p);
   return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
+// the fused selection's pages per thread (128 threads); 0: not fused
+int select_width(int32_t idx_dtype, int32_t q_dtype, int32_t max_pages, int32_t blocks) {
+  if (idx_dtype != BSP_FP8_E4M3 || q_dtype != BSP_FP8_E4M3 || blocks) return 0;
+  for (int w = 4; w <= 32; w *= 2)
+    if (max_pages <= 128 * w) return w;
+  return 0;
+}
+
 }  // namespace
+
+bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_pages, int32_t blocks) {
+  return select_width(idx_dtype, q_dtype, max_pages, blocks) != 0;
+}
 
 cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) {
   if (p.num_rows == 0 || p.max_pages == 0) return cudaSuccess;
   p.num_groups = (p.num_tokens + p.q_group - 1) / p.q_group;
   const int64_t max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+  const int sel = p.sel_counters ? select_width(p.idx_dtype, p.q_dtype, p.max_pages, p.sel.blocks) : 0;
+  if (p.sel_counters && !sel) return cudaErrorInvalidValue;  // the caller checks index_score_can_select
   switch (p.idx_dtype) {
     case BSP_BF16:
-      plan_key<BSP_BF16>(p, max_blocks, num_sms);
-      break;
+      return launch_key<BSP_BF16, 0>(p, max_blocks, num_sms, s);
     case BSP_FP8_E4M3:
-      if (p.q_dtype == BSP_FP8_E4M3)
-        plan_key<kFp8KeysE4m3Q>(p, max_blocks, num_sms);
-      else
-        plan_key<BSP_FP8_E4M3>(p, max_blocks, num_sms);
-      break;
+      if (p.q_dtype != BSP_FP8_E4M3) return launch_key<BSP_FP8_E4M3, 0>(p, max_blocks, num_sms, s);
+      switch (sel) {
+        case 4:
+          return launch_key<kFp8KeysE4m3Q, 4>(p, max_blocks, num_sms, s);
+        case 8:
+          return launch_key<kFp8KeysE4m3Q, 8>(p, max_blocks, num_sms, s);
+        case 16:
+          return launch_key<kFp8KeysE4m3Q, 16>(p, max_blocks, num_sms, s);
+        case 32:
+          return launch_key<kFp8KeysE4m3Q, 32>(p, max_blocks, num_sms, s);
+        default:
+          return launch_key<kFp8KeysE4m3Q, 0>(p, max_blocks, num_sms, s);
+      }
     default:
-      plan_key<BSP_MXFP4>(p, max_blocks, num_sms);
-  }
-  const int64_t cb = p.blocks_per_chunk;
-  const dim3 grid(static_cast<unsigned>(p.num_groups * p.hidx), static_cast<unsigned>((max_blocks + cb - 1) / cb));
-  switch (p.idx_dtype) {
-    case BSP_BF16:
-      return launch_key<BSP_BF16>(p, grid, s);
-    case BSP_FP8_E4M3:
-      return p.q_dtype == BSP_FP8_E4M3 ? launch_key<kFp8KeysE4m3Q>(p, grid, s) : launch_key<BSP_FP8_E4M3>(p, grid, s);
-    default:
-      return launch_key<BSP_MXFP4>(p, grid, s);
+      return launch_key<BSP_MXFP4, 0>(p, max_blocks, num_sms, s);
   }
 }
 

@@ -79,24 +79,6 @@ cudaError_t launch_row_lengths_decode(const int32_t* seq_lens, int32_t num_seqs,
 cudaError_t launch_row_lengths_prefill(const int32_t* req, const int32_t* pos, int32_t n, int32_t heads,
                                        int32_t* row_seq, int32_t* row_len, cudaStream_t s);
 
-struct IndexScoreParams {
-  int32_t idx_dtype, hidx;
-  const uint8_t* idx_base;
-  int64_t block_stride, num_blocks;
-  const void* q;
-  int32_t q_dtype;
-  const int32_t* block_table;
-  int32_t bt_stride;
-  const int32_t* row_seq;
-  const int32_t* row_len;
-  int32_t num_rows, num_tokens, q_group, max_pages;
-  int32_t blocks_per_chunk, num_groups, stages;  // filled by the launcher
-  int32_t seq_is_group;  // 1: rows are decode-ordered, group g is sequence g (no row_seq lookup first)
-  float* scores;
-  int32_t* err;
-};
-cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s);
-
 struct TopkParams {
   const float* scores;
   int32_t num_rows, max_pages;
@@ -112,6 +94,35 @@ struct TopkParams {
   int32_t* sparse_ctx;
 };
 cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s);
+
+struct IndexScoreParams {
+  int32_t idx_dtype, hidx;
+  const uint8_t* idx_base;
+  int64_t block_stride, num_blocks;
+  const void* q;
+  int32_t q_dtype;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* row_seq;
+  const int32_t* row_len;
+  int32_t num_rows, num_tokens, q_group, max_pages;
+  int32_t blocks_per_chunk, num_groups, stages;  // filled by the launcher
+  int32_t seq_is_group;  // 1: rows are decode-ordered, group g is sequence g (no row_seq lookup first)
+  float* scores;
+  int32_t* err;
+  // decode step, optional (NULL: off): the scorer also selects.  One int32
+  // per (group, index head), zero on entry and left zero: the last CTA of a
+  // group to finish its chunk selects the group's rows with `sel` (see
+  // index_score_can_select).
+  int32_t* sel_counters;
+  TopkParams sel;
+};
+cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s);
+// whether launch_index_score fuses the selection for these rows (else the
+// caller launches the selector)
+bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_pages, int32_t blocks);
+
+
 
 struct SparsePaParams {
   int32_t kv_dtype, hkv;

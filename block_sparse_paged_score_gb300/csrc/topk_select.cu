@@ -18,6 +18,7 @@
 // so the table comes out in ascending page order without a sort.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk_row.cuh"
 
 namespace bsp {
 
@@ -25,12 +26,6 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kSmemKeys = 16384;  // rows with more candidates read keys from global memory
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // exclusive prefix sum over the block; returns this thread's offset and the total
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& total) {
@@ -308,89 +303,11 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
 #define BSP_TOPK_WARP_MAX 128
 #endif
 
-// Radix select over keys held in registers by a CTA: thread t holds NK keys
-// of candidates first..first+NK-1 (valid below n_cand).  Four 8-bit passes,
-// most significant digit first, each with one shared-memory histogram (the
-// four are zeroed by the caller before its first __syncthreads) and one warp
-// scanning its 256 bins from the top, find tau, the need-th largest key, and
-// take_eq, how many keys equal to tau are taken.  Block-wide: every thread
-// of the CTA calls it.
-template <int NK>
-__device__ __forceinline__ void radix_select_regs(const uint32_t (&key)[NK], int first, int n_cand, int need,
-                                                  int (&s_hist)[4][256], uint32_t& s_digit, int& s_above, int warp,
-                                                  int lane, uint32_t& tau, int& take_eq) {
-  uint32_t prefix = 0, mask = 0;
-  int krem = need;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    __syncthreads();  // histograms zeroed; the previous pass's digit read
-#pragma unroll
-    for (int j = 0; j < NK; ++j)
-      if (first + j < n_cand && (key[j] & mask) == prefix) atomicAdd(&s_hist[pass][(key[j] >> shift) & 255], 1);
-    __syncthreads();
-    if (warp == 0) {
-      // lane owns bins 255-8*lane .. 248-8*lane (descending); find the digit
-      // where the running count from the top first reaches krem
-      int c[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = s_hist[pass][255 - 8 * lane - j];
-        sum += c[j];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - sum;  // keys in higher bins
-      if (run < krem && krem <= incl) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (run < krem && krem <= run + c[j]) {
-            s_digit = static_cast<uint32_t>(255 - 8 * lane - j);
-            s_above = run;
-          }
-          run += c[j];
-        }
-      }
-    }
-    __syncthreads();
-    krem -= s_above;
-    prefix |= s_digit << shift;
-    mask |= 255u << shift;
-  }
-  tau = prefix;
-  take_eq = krem;
-}
-
-// exclusive prefix over the CTA (in thread order) of a per-thread count
-// packed as (gt << 16) | eq; both fields stay below 2^16
-__device__ __forceinline__ int cta_exclusive_packed(int packed, int* s_warp, int warp, int lane) {
-  int x = packed;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  int before = x - packed;
-  for (int w = 0; w < warp; ++w) before += s_warp[w];
-  return before;
-}
-
-// One CTA of 256 threads per row of up to 256*KPT pages.  Thread t owns the
-// KPT consecutive pages t*KPT.. in registers (and the ids of the one or two
-// 128-token blocks they lie in, loaded up front).  A radix select of four
-// 8-bit passes (one shared-memory histogram per pass, one warp scans its 256
-// bins) finds tau, the need-th largest key, and how many keys equal to tau
-// are taken.  One block-wide scan of the packed per-thread counts (keys >
-// tau, keys == tau) then gives every thread the output slot of its first
-// selected page: the keys > tau before it, plus the ties before it up to the
-// number taken (the lower page wins a tie).  Pages come out in ascending
-// order with no sort.
+// One CTA of 256 threads per row of up to 256*KPT pages (select_row_cta).
+// Inside the decode step (rows_per_seq > 0) the row lengths come from the
+// step's first kernel, done before the scorer started: only the scores need
+// the wait, so the lengths, the unused tail of the outputs and the block ids
+// go first.  Every CTA still waits before it exits.
 constexpr int kCtaThreads = 256;
 
 template <int KPT>
@@ -399,99 +316,13 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
   __shared__ int s_warp[kCtaThreads / 32];
   __shared__ uint32_t s_digit;
   __shared__ int s_above;
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
-  // Inside the decode step (rows_per_seq > 0) the row lengths come from the
-  // step's first kernel, done before the scorer started: only the scores
-  // need the wait, so the lengths, the unused tail of the outputs and the
-  // block ids go first.  Every CTA still waits before it exits.
+  for (int i = threadIdx.x; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
   const bool in_step = p.rows_per_seq > 0;
   if (!in_step) {
     pdl_wait();  // scores (and the row lengths) come from earlier kernels
     pdl_trigger();
   }
-  const int max_len = p.max_pages * kPage;
-  const int L = min(max(p.row_len[r], 0), max_len);
-  const int n = (L + kPage - 1) / kPage;
-  const int kk = min(p.k_pages, n);
-  int32_t* ti = p.topk_idx + static_cast<int64_t>(r) * p.k_pages;
-  int32_t* bt = p.sparse_bt + static_cast<int64_t>(r) * p.k_pages;
-  for (int m = kk + tid; m < p.k_pages; m += kCtaThreads) ti[m] = bt[m] = -1;
-  if (kk == 0) {
-    if (tid == 0) p.sparse_ctx[r] = 0;
-    if (in_step) pdl_wait();
-    return;
-  }
-  const int n_cand = p.force_tail ? n - 1 : n;
-  const int need = p.force_tail ? kk - 1 : kk;
-  const bool all = need >= n_cand, none = need == 0, radix = !all && !none;
-
-  // independent loads: the ids of the blocks this thread's pages lie in
-  // (pages first.. first+KPT-1 span NB blocks from b0) and its scores
-  constexpr int NB = KPT >= kPagesPerSide ? KPT / kPagesPerSide : 1;
-  const int first = tid * KPT;
-  const int nblk = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
-  const int b0 = first / kPagesPerSide;
-  const int64_t bt_row = static_cast<int64_t>(p.rows_per_seq > 0 ? r / p.rows_per_seq : p.row_seq[r]) * p.bt_stride;
-  int32_t ids[NB];
-#pragma unroll
-  for (int k = 0; k < NB; ++k) ids[k] = b0 + k < nblk ? p.block_table[bt_row + b0 + k] * p.id_mul : 0;
-  if (in_step) {
-    pdl_wait();  // the scores
-    pdl_trigger();
-  }
-  const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
-  uint32_t key[KPT];
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) key[j] = (radix && first + j < n_cand) ? order_key(srow[first + j]) : 0u;
-
-  uint32_t tau = 0;
-  int take_eq = 0;
-  if (radix) radix_select_regs<KPT>(key, first, n_cand, need, s_hist, s_digit, s_above, warp, lane, tau, take_eq);
-
-  // (keys > tau, keys == tau) of this thread, scanned over the block in page order
-  int gt = 0, eq = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const bool valid = first + j < n_cand;
-    gt += valid && (all || (radix && key[j] > tau));
-    eq += valid && radix && key[j] == tau;
-  }
-  const int before = cta_exclusive_packed((gt << 16) | eq, s_warp, warp, lane);
-  int eqr = before & 0xFFFF;
-  int pos = (before >> 16) + min(eqr, take_eq);
-  bool tail_sel = false;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int pg = first + j;
-    const bool valid = pg < n_cand;
-    const bool is_eq = valid && radix && key[j] == tau;
-    const bool sel = valid && !none && (all || (radix && key[j] > tau) || (is_eq && eqr < take_eq));
-    eqr += is_eq;
-    if (sel && pos < need) {
-      ti[pos] = pg;
-      bt[pos] = ids[KPT >= kPagesPerSide ? j / kPagesPerSide : 0] + pg % kPagesPerSide;  // first % 8 == 0 there
-      ++pos;
-    }
-    if (pg == n - 1) tail_sel = sel;
-  }
-  // the owner of page n-1 finishes the row: the forced tail entry, and the
-  // context length (the tail page, if selected, is the last entry)
-  if (first <= n - 1 && n - 1 < first + KPT) {
-    const int pg = n - 1;
-    const int tail_len = L - kPage * (n - 1);
-    if (p.force_tail) {
-      ti[kk - 1] = pg;
-      int32_t id = ids[0];
-#pragma unroll
-      for (int k = 1; k < NB; ++k)
-        if (pg / kPagesPerSide - b0 == k) id = ids[k];
-      bt[kk - 1] = id + pg % kPagesPerSide;
-      p.sparse_ctx[r] = kPage * (kk - 1) + tail_len;
-    } else {
-      p.sparse_ctx[r] = kPage * (kk - 1) + (tail_sel ? tail_len : kPage);
-    }
-  }
+  select_row_cta<KPT, kCtaThreads>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
 }
 
 // 128-token blocks as the unit of selection (pages_per_block = 8).  One CTA

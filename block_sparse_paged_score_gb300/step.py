@@ -19,7 +19,12 @@ from . import bsp
 
 
 class DecodeStep:
-    def __init__(self, w, kv, idx, block_table, device="cuda", flags=bsp.FORCE_TAIL):
+    """select_in_scorer: hand the step a zeroed counter per (sequence, index
+    head) so that the scorer's last CTA of each sequence selects its rows
+    (where the library supports it; the outputs are the same, the step is
+    slower on the benchmark workloads, so it is off by default)."""
+
+    def __init__(self, w, kv, idx, block_table, device="cuda", flags=bsp.FORCE_TAIL, select_in_scorer=False):
         self.w = w
         self.kv, self.idx = kv, idx
         self.block_table = block_table
@@ -49,6 +54,8 @@ class DecodeStep:
                                                  self.sparse_ctx.data_ptr())
         a.out, a.ws, a.ws_bytes, a.dev_err = self.out.data_ptr(), self.ws.data_ptr(), self.ws.numel(), \
             self.dev_err.data_ptr()
+        self.sel_counters = torch.zeros(max(1, w.num_decode * w.hidx), dtype=torch.int32, device=device)
+        a.sel_counters = self.sel_counters.data_ptr() if select_in_scorer else None
 
     def run(self, k_new, v_new, idx_k_new, slot, q, idx_q, seq_lens, events=None, stream=None):
         """Device tensors in; fills self.out (and the intermediate buffers)."""

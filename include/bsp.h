@@ -394,6 +394,15 @@ typedef struct bsp_decode_step_args {
   void* ws;                   /* bsp_sparse_pa_decode_workspace_bytes(rows, k_pages, G) */
   size_t ws_bytes;
   int32_t* dev_err;
+  /* optional (NULL: a separate selector launch): int32 [num_seqs * Hidx],
+   * zeroed once by the caller and left zero by every step.  The scorer's
+   * last CTA of each (sequence, index head) then selects that sequence's
+   * rows itself, one launch fewer -- the same outputs bit for bit, but
+   * every scorer CTA then waits for a counter round trip before it retires
+   * and one CTA selects all of a sequence's rows, so on large batches the
+   * step is slower.  Used for fp8 index caches with e4m3 index queries,
+   * max_pages <= 4096 and page-granular selection; otherwise ignored. */
+  int32_t* sel_counters;
 } bsp_decode_step_args;
 
 bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* events, bsp_stream_t stream);

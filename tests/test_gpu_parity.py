@@ -433,3 +433,28 @@ def test_host_step_zero_copy_matches_device_step(bsp, name):
         torch.cuda.synchronize()
         assert st.dev_err.item() == 0
         assert torch.equal(out, ref.cpu()), zc
+
+
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2"])
+def test_decode_step_selection_in_scorer(bsp, name):
+    """With sel_counters the scorer's last CTA of each sequence selects its
+    rows: the same scores, tables and output as the step with a separate
+    selector, on two steps in a row (the counters are left at zero)."""
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides(name)
+    k, v, ik, slot = w.step_tokens()
+    args = (g.t(k), g.t(v), g.t(ik), g.t(slot), g.q_bf16, g.idx_q_bf16, g.t(w.decode_lens))
+    a = step.DecodeStep(w, g.kv, g.idx, g.block_table, select_in_scorer=False)
+    b = step.DecodeStep(w, g.kv, g.idx, g.block_table, select_in_scorer=True)
+    launches = []
+    for _ in range(2):
+        a.run(*args)
+        n0 = bsp.launch_count()
+        b.run(*args)
+        launches.append(bsp.launch_count() - n0)
+        torch.cuda.synchronize()
+        assert a.dev_err.item() == 0 and b.dev_err.item() == 0
+        for x in ("scores", "topk_idx", "sparse_bt", "sparse_ctx", "out"):
+            assert torch.equal(getattr(a, x), getattr(b, x)), x
+        assert int(b.sel_counters.abs().sum().item()) == 0
+    assert launches == [3, 3]  # prep, scorer with selection, attention
