@@ -108,7 +108,7 @@ __device__ __forceinline__ void select_unit(const IndexScoreParams& p, const int
   int& s_above = *reinterpret_cast<int*>(smem + 4096 + 20);
   for (int j = 0; j < ntok; ++j) {
     for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&hist[0][0])[i] = 0;
-    select_row_cta<SEL, 128>(p.sel, s_row[j], hist, s_warp, s_digit, s_above, false);
+    select_row_cta<SEL, 128, true>(p.sel, s_row[j], hist, s_warp, s_digit, s_above, false);
     __syncthreads();  // the next row reuses the histograms and the scan slots
   }
   if (threadIdx.x == 0) p.sel_counters[blockIdx.x] = 0;

@@ -103,9 +103,9 @@ __device__ __forceinline__ int cta_exclusive_packed(int packed, int* s_warp, int
 // number taken (the lower page wins a tie).  Pages come out in ascending
 // order with no sort.  s_hist must be zero on entry.  With wait_scores the
 // CTA waits for the kernel before (griddepcontrol) just before it reads the
-// scores, and before it returns early.  Scores are read through L2 (they may
-// have been written by other CTAs of the same kernel).
-template <int KPT, int NT>
+// scores, and before it returns early.  L2_ONLY reads the scores through L2
+// (for scores written by other CTAs of the same kernel).
+template <int KPT, int NT, bool L2_ONLY>
 __device__ __forceinline__ void select_row_cta(const TopkParams& p, int r, int (&s_hist)[4][256], int* s_warp,
                                                uint32_t& s_digit, int& s_above, bool wait_scores) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -142,7 +142,8 @@ __device__ __forceinline__ void select_row_cta(const TopkParams& p, int r, int (
   const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
   uint32_t key[KPT];
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) key[j] = (radix && first + j < n_cand) ? order_key(__ldcg(srow + first + j)) : 0u;
+  for (int j = 0; j < KPT; ++j)
+    key[j] = (radix && first + j < n_cand) ? order_key(L2_ONLY ? __ldcg(srow + first + j) : srow[first + j]) : 0u;
 
   uint32_t tau = 0;
   int take_eq = 0;

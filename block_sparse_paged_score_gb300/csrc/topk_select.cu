@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
     pdl_wait();  // scores (and the row lengths) come from earlier kernels
     pdl_trigger();
   }
-  select_row_cta<KPT, kCtaThreads>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
+  select_row_cta<KPT, kCtaThreads, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
 }
 
 // 128-token blocks as the unit of selection (pages_per_block = 8).  One CTA
