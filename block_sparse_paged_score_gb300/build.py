@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libbsp.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "kv_write.cu", "index_score.cu", "index_score_prefill_tc.cu", "topk_select.cu", "sparse_pa.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "kv_write.cu", "index_score.cu", "index_score_mx_tc.cu", "index_score_prefill_tc.cu",
+           "topk_select.cu", "sparse_pa.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

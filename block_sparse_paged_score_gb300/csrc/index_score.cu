@@ -414,10 +414,39 @@ bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_page
   return select_width(idx_dtype, q_dtype, max_pages, blocks) != 0;
 }
 
+// MXFP4 keys with e4m3 queries on tcgen05: the same chunk grid, planned with
+// that kernel's occupancy and a 4-deep ring
+void plan_mx_tc(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
+  const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
+  const double start_blocks = kStartBytes / kMxField;
+  const int64_t resident = static_cast<int64_t>(index_score_mx_tc_occupancy()) * num_sms;
+  double best = 0.0;
+  for (int cb = 1; cb <= 32; ++cb) {
+    const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
+    const int64_t waves = (ctas + resident - 1) / resident;
+    const double cost = static_cast<double>(waves) * (cb + start_blocks);
+    if (cb == 1 || cost < best) {
+      best = cost;
+      p.blocks_per_chunk = cb;
+      p.stages = 4;
+    }
+    if (cb >= max_blocks) break;
+  }
+}
+
 cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) {
   if (p.num_rows == 0 || p.max_pages == 0) return cudaSuccess;
   p.num_groups = (p.num_tokens + p.q_group - 1) / p.q_group;
   const int64_t max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
+#ifndef BSP_IDX_MX_TC
+#define BSP_IDX_MX_TC 1
+#endif
+  if (BSP_IDX_MX_TC && !p.sel_counters && index_score_mx_tc_supported(p)) {
+    plan_mx_tc(p, max_blocks, num_sms);
+    const int64_t cb = p.blocks_per_chunk;
+    return launch_index_score_mx_tc(
+        p, dim3(static_cast<unsigned>(p.num_groups * p.hidx), static_cast<unsigned>((max_blocks + cb - 1) / cb)), s);
+  }
   const int sel = p.sel_counters ? select_width(p.idx_dtype, p.q_dtype, p.max_pages, p.sel.blocks) : 0;
   if (p.sel_counters && !sel) return cudaErrorInvalidValue;  // the caller checks index_score_can_select
   switch (p.idx_dtype) {

@@ -24,16 +24,16 @@
 // or past the row's causal length, max-pools 16 keys into a page score and
 // stores 8 pages per row per tile.  Accumulator double-buffering lets the
 // MMAs of the next tile run under the epilogue of this one.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace bsp {
 
 namespace {
 
+// instruction descriptor: A = B = e4m3, N = 256 keys, M = 128 queries
+constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE4m3, kFmtE4m3, 256, 128);
 constexpr int kStages = 4;
 constexpr int kKeyBlocksPerCta = 64;
 constexpr int kEpiWarps = 8;
@@ -59,61 +59,6 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
   L.bars = reinterpret_cast<uint64_t*>(L.scales + 2 * 256);
   L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 16);
   return L;
-}
-
-// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 B apart (SBO), leading offset unused for a swizzled K-major operand.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);  // start address
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset
-  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                  // SWIZZLE_128B
-  return d;
-}
-
-// instruction descriptor: kind::f8f6f4, D fp32, A = B = e4m3, both K-major,
-// N = 256, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -256,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b_addr = smem_u32(sm.b + st * 2 * kTileBytes);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma_f8(tmem + buf * 256, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), k > 0);
+          umma_f8(tmem + buf * 256, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), kIdesc, k > 0);
         umma_commit(&b_empty[st]);
         umma_commit(&acc_full[buf]);
         if (j + kStages < ntiles) {
@@ -333,37 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {128, rows};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, 128};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t s) {
   CUtensorMap tq, tk;
   const uint64_t key_rows = static_cast<uint64_t>(p.num_blocks) * (p.block_stride / 128);
-  if (!make_map(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map(&tk, p.idx_base, key_rows))
+  if (!make_map_u8(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map_u8(&tk, p.idx_base, key_rows))
     return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {

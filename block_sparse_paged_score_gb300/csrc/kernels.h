@@ -118,6 +118,11 @@ struct IndexScoreParams {
   TopkParams sel;
 };
 cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s);
+// the tcgen05 scorer for MXFP4 keys and e4m3 queries (launch_index_score
+// takes it when supported)
+bool index_score_mx_tc_supported(const IndexScoreParams& p);
+int index_score_mx_tc_occupancy();
+cudaError_t launch_index_score_mx_tc(const IndexScoreParams& p, dim3 grid, cudaStream_t s);
 // whether launch_index_score fuses the selection for these rows (else the
 // caller launches the selector)
 bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_pages, int32_t blocks);
