@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libbsp.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "kv_write.cu", "index_score.cu", "index_score_mx_tc.cu", "index_score_prefill_tc.cu",
-           "topk_select.cu", "sparse_pa.cu", "noalloc.cu"]
+           "index_score_prefill_mx_tc.cu", "topk_select.cu", "sparse_pa.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -243,8 +243,10 @@ bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q
                                    int32_t* dev_err, bsp_stream_t stream) {
   bsp_status st = check_idx(idx);
   if (st != BSP_OK) return st;
-  if (idx->dtype != BSP_FP8_E4M3 || q_dtype != BSP_FP8_E4M3 || idx->num_heads != 1) return BSP_ERR_UNSUPPORTED;
-  if (idx->block_stride_bytes % 128) return BSP_ERR_UNSUPPORTED;
+  const bool mx = idx->dtype == BSP_MXFP4;
+  if ((idx->dtype != BSP_FP8_E4M3 && !mx) || q_dtype != BSP_FP8_E4M3 || idx->num_heads != 1)
+    return BSP_ERR_UNSUPPORTED;
+  if (idx->block_stride_bytes % (mx ? 64 : 128)) return BSP_ERR_UNSUPPORTED;
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1 || num_chunks < 0 || max_tiles < 0) return BSP_ERR_INVALID_ARG;
   if (static_cast<int64_t>(max_pages) > static_cast<int64_t>(bt_stride) * 8) return BSP_ERR_INVALID_ARG;
   if (num_rows == 0 || num_chunks == 0 || max_tiles == 0) return BSP_OK;
@@ -266,7 +268,8 @@ bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q
   p.max_pages = max_pages;
   p.scores = scores;
   p.err = dev_err;
-  cudaError_t e = launch_index_score_prefill(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = mx ? launch_index_score_prefill_mx(p, reinterpret_cast<cudaStream_t>(stream))
+                     : launch_index_score_prefill(p, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return BSP_ERR_UNSUPPORTED;
   st = cuda_status(e);
   if (st == BSP_OK) ++g_launches;

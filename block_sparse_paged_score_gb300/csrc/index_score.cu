@@ -418,7 +418,10 @@ bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_page
 // that kernel's occupancy and a 4-deep ring
 void plan_mx_tc(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
-  const double start_blocks = kStartBytes / kMxField;
+#ifndef BSP_MXTC_START_X10
+#define BSP_MXTC_START_X10 0
+#endif
+  const double start_blocks = BSP_MXTC_START_X10 ? BSP_MXTC_START_X10 / 10.0 : kStartBytes / kMxField;
   const int64_t resident = static_cast<int64_t>(index_score_mx_tc_occupancy()) * num_sms;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {

@@ -37,7 +37,11 @@ namespace bsp {
 
 namespace {
 
-constexpr int kStages = 4;
+#ifndef BSP_MXTC_STAGES
+#define BSP_MXTC_STAGES 3
+#endif
+constexpr int kStages = BSP_MXTC_STAGES;
+constexpr int kScaleSlots = kStages + 2;  // a block's scales live until its epilogue is done
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (1 + kEpiWarps);
 constexpr int kN = 16;  // query columns: the group's rows, zero-padded
@@ -46,13 +50,13 @@ constexpr int kKeyTile = 128 * 128;                      // shared bytes of one 
 constexpr uint32_t kKeyTx = 128 * 64;  // the transaction count: the packed bytes read, not the padded ones
 constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE2m1, kFmtE4m3, kN, 128);
 constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kKeyTile + kN * 128 /*queries*/ +
-                           2 * 512 /*scales*/ + 16 * 8 /*barriers*/ + 16;
+                           kScaleSlots * 512 /*scales*/ + 24 * 8 /*barriers*/ + 16;
 
 struct SmemLayout {
   uint8_t* keys;    // [stage][128 rows][128 B]
   uint8_t* q;       // [16 rows][128 B]
-  uint8_t* scales;  // [2][128 tokens][4]
-  uint64_t* bars;   // full[S], empty[S], acc_full[2], acc_empty[2], scale_full[2]
+  uint8_t* scales;  // [kScaleSlots][128 tokens][4]
+  uint64_t* bars;   // full[S], empty[S], acc_full[2], acc_empty[2], scale_full[kScaleSlots]
   uint32_t* tmem_slot;
 };
 
@@ -62,8 +66,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
   L.keys = base;
   L.q = base + kStages * kKeyTile;
   L.scales = L.q + kN * 128;
-  L.bars = reinterpret_cast<uint64_t*>(L.scales + 2 * 512);
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 16);
+  L.bars = reinterpret_cast<uint64_t*>(L.scales + kScaleSlots * 512);
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 24);
   return L;
 }
 
@@ -109,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * kEpiWarps);
-      mbar_init(&scale_full[i], 1);
     }
+    for (int i = 0; i < kScaleSlots; ++i) mbar_init(&scale_full[i], 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -162,26 +166,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint8_t* field0 = p.idx_base + static_cast<int64_t>(h) * kMxField;
-      auto load_keys = [&](int i) {
-        const int st = i % kStages;
+      // block i: its keys into ring slot i % S, its e8m0 scales into scale
+      // slot i % (S+2) -- whose last user, block i-S-2, has finished its
+      // epilogue once the MMAs of block i-S were issued
+      auto load_block = [&](int i) {
+        const int st = i % kStages, ss = i % kScaleSlots;
         const int64_t row = (static_cast<int64_t>(s_bid[i]) * p.block_stride + static_cast<int64_t>(h) * kMxField) / 64;
         mbar_arrive_expect_tx(&full[st], kKeyTx);
         tma_load_2d(sm.keys + st * kKeyTile, &tmap_k, 0, static_cast<int>(row), &full[st]);
+        fence_proxy_async();  // the epilogue's reads of the slot's previous scales
+        mbar_arrive_expect_tx(&scale_full[ss], 512);
+        bulk_g2s(sm.scales + ss * 512, field0 + static_cast<int64_t>(s_bid[i]) * p.block_stride + kMxScaleOff, 512,
+                 &scale_full[ss]);
       };
       bool alive = true;
-      for (int i = 0; i < min(kStages, nb); ++i) load_keys(i);
+      for (int i = 0; i < min(kStages, nb); ++i) load_block(i);
       const uint32_t q_addr = smem_u32(sm.q);
       for (int i = 0; i < nb && alive; ++i) {
         const int st = i % kStages, buf = i & 1;
         alive = mbar_wait(&full[st], (i / kStages) & 1, p.err) &&
                 mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, p.err);
         if (!alive) break;
-        // this block's e8m0 scales into the accumulator's scale slot (the
-        // epilogue of block i-2 has released it)
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&scale_full[buf], 512);
-        bulk_g2s(sm.scales + buf * 512, field0 + static_cast<int64_t>(s_bid[i]) * p.block_stride + kMxScaleOff, 512,
-                 &scale_full[buf]);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t k_addr = smem_u32(sm.keys + st * kKeyTile);
 #pragma unroll
@@ -190,9 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   kIdesc, 0);
         umma_commit(&empty[st]);
         umma_commit(&acc_full[buf]);
-        if (i + kStages < nb) {
-          alive = mbar_wait(&empty[st], (i / kStages) & 1, p.err);
-          if (alive) load_keys(i + kStages);
+        // refill the previous block's slot: its MMAs were issued an iteration
+        // ago, so this wait overlaps the ones just issued
+        const int j = i - 1;
+        if (j >= 0 && j + kStages < nb) {
+          alive = mbar_wait(&empty[j % kStages], (j / kStages) & 1, p.err);
+          if (alive) load_block(j + kStages);
         }
       }
       // nothing may still be writing shared memory or TMEM when the CTA
@@ -206,14 +214,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool alive = true;
     for (int i = 0; i < nb && alive; ++i) {
       const int buf = i & 1;
-      alive = mbar_wait(&scale_full[buf], (i >> 1) & 1, p.err) && mbar_wait(&acc_full[buf], (i >> 1) & 1, p.err);
+      const int ss = i % kScaleSlots;
+      alive = mbar_wait(&scale_full[ss], (i / kScaleSlots) & 1, p.err) &&
+              mbar_wait(&acc_full[buf], (i >> 1) & 1, p.err);
+      alive = __all_sync(0xffffffffu, alive);  // tcgen05.ld below is warp-wide
       if (!alive) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kAccCols;
       float a[4][8];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld8(taddr + kN * g, a[g]);  // the group's first 8 query columns
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(sm.scales + buf * 512 + 4 * t);
+      tmem_ld8x4(taddr, kN, a);  // each group's first 8 query columns
+      const uint32_t sc = *reinterpret_cast<const uint32_t*>(sm.scales + ss * 512 + 4 * t);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       mbar_arrive(&acc_empty[buf]);
       float f[4];

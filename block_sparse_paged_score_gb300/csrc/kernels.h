@@ -176,5 +176,7 @@ struct PrefillScoreParams {
   int32_t* err;
 };
 cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t s);
+// the same for an MXFP4 index cache (e2m1 keys, e8m0 scales per 32 dims)
+cudaError_t launch_index_score_prefill_mx(const PrefillScoreParams& p, cudaStream_t s);
 
 }  // namespace bsp

@@ -81,6 +81,23 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 8 consecutive fp32 columns at each of taddr, taddr + stride, + 2*stride,
+// + 3*stride: four loads in flight, one wait
+__device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, uint32_t stride, float (&v)[4][8]) {
+  uint32_t r[4][8];
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[g][0]), "=r"(r[g][1]), "=r"(r[g][2]), "=r"(r[g][3]), "=r"(r[g][4]), "=r"(r[g][5]),
+                   "=r"(r[g][6]), "=r"(r[g][7])
+                 : "r"(taddr + g * stride));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[g][i] = __uint_as_float(r[g][i]);
+}
+
 // ---- host: tensor maps -------------------------------------------------------
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -225,8 +225,10 @@ bsp_status bsp_index_score(const bsp_index_cache* idx, const void* idx_q, int32_
  * scorer).  Rows of one chunk are consecutive query tokens of one sequence.
  *   cu_tokens int32 [num_chunks+1]: token offsets of the chunks (device)
  *   max_tiles host upper bound on sum_c ceil(tokens_c / 128)
- *   idx->dtype must be BSP_FP8_E4M3 and q_dtype BSP_FP8_E4M3, one index
- *   head (idx->num_heads == 1); else BSP_ERR_UNSUPPORTED.
+ *   idx->dtype BSP_FP8_E4M3 or BSP_MXFP4 (e2m1 keys read by the tensor core
+ *   from 4-bit-unpacking TMA loads, the e8m0 group scales applied to one
+ *   accumulator per 32-dim group), q_dtype BSP_FP8_E4M3, one index head
+ *   (idx->num_heads == 1); else BSP_ERR_UNSUPPORTED.
  * Other arguments as bsp_index_score (rows = tokens).
  * ---------------------------------------------------------------------- */
 bsp_status bsp_index_score_prefill(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,

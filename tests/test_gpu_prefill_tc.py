@@ -1,6 +1,7 @@
-"""Parity of the tcgen05 prefill index scorer with the oracle (GPU required):
-fp8 index cache, e4m3 index queries, chunks of consecutive query tokens with
-causal lengths, partial 128-row tiles, several 8192-key ranges and pad rows."""
+"""Parity of the tcgen05 prefill index scorers with the oracle (GPU required):
+fp8 and MXFP4 index caches, e4m3 index queries, chunks of consecutive query
+tokens with causal lengths, partial 128-row tiles, several 8192-key ranges and
+pad rows."""
 import numpy as np
 import pytest
 import torch
@@ -24,6 +25,16 @@ CASES = {
     "wide": dict(name="pre-wide", seed=23, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
                  hkv=1, group=16, k_pages=32, q_len=1, decode_lens=[100],
                  prefill_chunks=[(9100, 300), (17000, 260)], pad_seqs=1, pad_q_len=4),
+    # MXFP4 index cache (e2m1 keys, e8m0 per 32 dims): the same shapes
+    "mx_small": dict(name="pre-mx-small", seed=24, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8,
+                     idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=16, q_len=1, decode_lens=[40],
+                     prefill_chunks=[(384, 200), (700, 300)], pad_seqs=1, pad_q_len=4),
+    "mx_ranges": dict(name="pre-mx-ranges", seed=25, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8,
+                      idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=32, q_len=1, decode_lens=[5000],
+                      prefill_chunks=[(3000, 700), (5200, 1100), (128, 128)], pad_seqs=2, pad_q_len=4),
+    "mx_wide": dict(name="pre-mx-wide", seed=26, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8,
+                    idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=32, q_len=1, decode_lens=[100],
+                    prefill_chunks=[(9100, 300), (17000, 260)], pad_seqs=1, pad_q_len=4),
 }
 
 
