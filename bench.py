@@ -5,7 +5,7 @@
 A step is one pass of the whole path over one batch: write the step's new
 tokens into the caches, cast the queries the writer emits as e4m3, row
 lengths, index scores, top-k with the emitted sparse table, attention (split-K
-+ merge).  The workload is one of the five seeded synthetic configurations
++ merge).  The workload is one of the seeded synthetic configurations
 (default 2: 32 fp8 sequences of 4096..8192 tokens, 16 query heads per KV
 head, top-128 pages).
 
@@ -385,7 +385,10 @@ def run_ours(args):
     attn_bytes = attention_algorithmic_bytes(w, ctx_total)
     score_s = statistics.mean(score_ms) / 1e3
     attn_s = statistics.mean(attn_ms) / 1e3
-    per = {"index_score": (score_bytes, score_s, "index_score_kernel", ["index_score.cu", "common.cuh"]),
+    # MXFP4 keys with e4m3 queries run the tcgen05 scorer
+    idx_kernel = (("index_score_mx_tc_kernel", ["index_score_mx_tc.cu", "tcgen05.cuh", "common.cuh"])
+                  if w.idx_dtype == 2 and w.idx_q_dtype == 1 else ("index_score_kernel", ["index_score.cu", "common.cuh"]))
+    per = {"index_score": (score_bytes, score_s) + idx_kernel,
            "sparse_pa": (attn_bytes, attn_s, "sparse_pa_kernel", ["sparse_pa.cu", "common.cuh"])}
     kernels = {}
     for name, (nbytes, secs, kname, files) in per.items():

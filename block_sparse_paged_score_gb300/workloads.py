@@ -12,7 +12,7 @@ per element and u ~ N(0, 0.5) per 32-element group, so that the groups span
 a range of shared exponents.  Every (kind, sequence, 128-token block) has a
 generator of its own, so any block can be regenerated alone.
 
-The five named workloads restate the shapes of the pages' deployments
+The named workloads restate the shapes of the pages' deployments
 (MiniMax-M3 sparse decode with 128-token blocks and 16-token pages, one KV
 head and one index head per rank, 16 query heads per KV head, top-k of 2048
 tokens) as concrete seeded inputs; no dataset is involved.
@@ -41,6 +41,13 @@ CONFIGS = {
             hkv=1, group=16, k_pages=128, q_len=1, decode_lens=[131072] * 64),
     5: dict(name="fp8-mixed-64dec-4x4096pre-8pad", seed=1005, kv_dtype=FP8, idx_dtype=FP8, q_dtype=BF16,
             idx_q_dtype=FP8, hkv=1, group=16, k_pages=128, q_len=1, decode_lens=("uniform", 64, 1024, 65536),
+            prefill_chunks=[(16384, 4096), (32768, 4096), (49152, 4096), (65536, 4096)],
+            pad_seqs=2, pad_q_len=4),
+    # the chunked-prefill batch above with an MXFP4 index cache (the MXFP4
+    # prefill scorer's workload)
+    6: dict(name="fp8kv-mxfp4idx-mixed-64dec-4x4096pre-8pad", seed=1006, kv_dtype=FP8, idx_dtype=MXFP4,
+            q_dtype=BF16, idx_q_dtype=FP8, hkv=1, group=16, k_pages=128, q_len=1,
+            decode_lens=("uniform", 64, 1024, 65536),
             prefill_chunks=[(16384, 4096), (32768, 4096), (49152, 4096), (65536, 4096)],
             pad_seqs=2, pad_q_len=4),
 }

@@ -56,10 +56,10 @@ def test_host_validation_without_a_gpu():
     assert L.bsp_kv_cache_interleaved(bsp.FP8_E4M3, 1, fake + 8, 128, 0.5, 0.5, C.byref(d)) == 1  # misaligned
     ic = bsp.IndexCacheDesc()
     assert L.bsp_index_cache_packed(bsp.FP8_E4M3, 1, fake, 16, C.byref(ic)) == 0
-    # q_group out of range and an MXFP4 prefill scorer are refused before any launch
+    # q_group out of range and a prefill scorer with bf16 queries are refused before any launch
     assert L.bsp_index_score(C.byref(ic), fake, bsp.FP8_E4M3, fake, 4, fake, fake, 4, 9, 8, fake, None, None) == 2
     ic2 = bsp.IndexCacheDesc()
     assert L.bsp_index_cache_packed(bsp.MXFP4, 1, fake, 16, C.byref(ic2)) == 0
-    assert L.bsp_index_score_prefill(C.byref(ic2), fake, bsp.FP8_E4M3, fake, 4, fake, fake, 4, fake, 1, 1, 8, fake,
+    assert L.bsp_index_score_prefill(C.byref(ic2), fake, bsp.BF16, fake, 4, fake, fake, 4, fake, 1, 1, 8, fake,
                                      None, None) == 2
     assert L.bsp_topk_select(fake, 4, 8, fake, fake, fake, 1, 0, 0, 1, fake, fake, fake, None) == 1  # k_pages 0

@@ -1,6 +1,6 @@
 """Parity at the benchmark's full sizes (GPU required): each workload's step
 runs exactly as bench.py runs it -- the CUDA writer fills every sequence's
-caches, then one DecodeStep (workloads 2-4) or MixedStep (workload 5) -- and
+caches, then one DecodeStep (workloads 2-4) or MixedStep (workloads 5-6) -- and
 a sample of rows is checked against the oracle, which writes and scores only
 the sampled sequences:
   cache bytes of the sampled sequences' blocks equal, byte for byte;
@@ -34,7 +34,7 @@ def _sample_rows(w, rng):
     return np.array(sorted(rows), np.int32)
 
 
-@pytest.mark.parametrize("config", [2, 3, 4, 5])
+@pytest.mark.parametrize("config", [2, 3, 4, 5, 6])
 def test_full_size_step_on_sampled_rows(config):
     from block_sparse_paged_score_gb300 import bsp, step
     w = W.workload(config)
