@@ -449,6 +449,8 @@ def run_ours(args):
         modes = {"copy_engine": step.HostDecodeStep(st, host, device=dev)}
         if not mixed:
             modes["zero_copy"] = step.HostDecodeStep(st, host, device=dev, zero_copy=True)
+            modes["copy_in_zero_out"] = step.HostDecodeStep(st, host, device=dev, inputs="copy", output="zero")
+            modes["zero_in_copy_out"] = step.HostDecodeStep(st, host, device=dev, inputs="zero", output="copy")
         res = {m: time_host(hs) for m, hs in modes.items()}
         best = max(res, key=lambda m: res[m]["value"])
         e2e = dict(res[best], transfer=best, modes=res)

@@ -72,19 +72,22 @@ class HostDecodeStep:
     """End-to-end step: pinned host inputs -> device -> step -> host output.
 
     The step's inputs sit back to back (256-byte aligned) in one pinned host
-    buffer.  With zero_copy=False a step makes one host-to-device copy of all
-    of them and one device-to-host copy of the attention output.  With
-    zero_copy=True (a DecodeStep only) no copy is issued: the step's kernels
-    read their inputs straight from the pinned buffer and the attention writes
-    its output straight into pinned host memory -- pinned memory is mapped
-    into the device's address space, and on a Grace-Blackwell node these
-    loads and stores cross the NVLink-C2C link."""
+    buffer.  `inputs` and `output` each choose how the bytes cross the link:
+      "copy": one copy-engine copy (host-to-device of all the inputs, or
+              device-to-host of the attention output) on the step's stream;
+      "zero": no copy -- the step's kernels load the inputs straight from the
+              pinned buffer, or the attention stores its output straight
+              into pinned host memory (pinned memory is mapped into the
+              device's address space; on a Grace-Blackwell node these loads
+              and stores cross NVLink-C2C).  A DecodeStep only.
+    zero_copy=True is inputs="zero", output="zero"."""
 
-    def __init__(self, step, host_inputs, device="cuda", zero_copy=False):
+    def __init__(self, step, host_inputs, device="cuda", zero_copy=False, inputs=None, output=None):
         self.step = step
-        self.zero_copy = zero_copy
-        if zero_copy and not isinstance(step, DecodeStep):
-            raise ValueError("zero_copy needs a DecodeStep")
+        self.inputs = inputs or ("zero" if zero_copy else "copy")
+        self.output = output or ("zero" if zero_copy else "copy")
+        if "zero" in (self.inputs, self.output) and not isinstance(step, DecodeStep):
+            raise ValueError("zero-copy transfer needs a DecodeStep")
         offs, total = {}, 0
         for k, v in host_inputs.items():
             offs[k] = total
@@ -92,16 +95,13 @@ class HostDecodeStep:
         self.nbytes = total
         self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
         self.dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
-        self.dev = {}
+        self.dev, self.host = {}, {}
         for k, v in host_inputs.items():
             n = v.numel() * v.element_size()
             self.host_buf[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
             self.dev[k] = self.dev_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
-        self.out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        self.host = {}
-        for k, v in host_inputs.items():
-            n = v.numel() * v.element_size()
             self.host[k] = self.host_buf[offs[k]:offs[k] + n].view(v.dtype).view(v.shape)
+        self.out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
 
     @property
     def h2d_bytes(self):
@@ -113,20 +113,21 @@ class HostDecodeStep:
 
     def run(self, stream=None):
         s = stream if stream is not None else torch.cuda.current_stream()
-        if self.zero_copy:
-            h, a = self.host, self.step.args
-            dev_out = a.out
-            a.out = self.out_host.data_ptr()
-            try:
-                self.step.run(h["k"], h["v"], h["idx_k"], h["slot"], h["q"], h["idx_q"], h["seq_lens"], stream=s)
-            finally:
-                a.out = dev_out
-            return self.out_host
         with torch.cuda.stream(s):
-            self.dev_buf.copy_(self.host_buf, non_blocking=True)
-            d = self.dev
-            self.step.run(d["k"], d["v"], d["idx_k"], d["slot"], d["q"], d["idx_q"], d["seq_lens"], stream=s)
-            self.out_host.copy_(self.step.out, non_blocking=True)
+            if self.inputs == "copy":
+                self.dev_buf.copy_(self.host_buf, non_blocking=True)
+            d = self.dev if self.inputs == "copy" else self.host
+            if self.output == "zero":
+                a = self.step.args
+                dev_out = a.out
+                a.out = self.out_host.data_ptr()
+                try:
+                    self.step.run(d["k"], d["v"], d["idx_k"], d["slot"], d["q"], d["idx_q"], d["seq_lens"], stream=s)
+                finally:
+                    a.out = dev_out
+            else:
+                self.step.run(d["k"], d["v"], d["idx_k"], d["slot"], d["q"], d["idx_q"], d["seq_lens"], stream=s)
+                self.out_host.copy_(self.step.out, non_blocking=True)
         return self.out_host
 
 

@@ -427,12 +427,13 @@ def test_host_step_zero_copy_matches_device_step(bsp, name):
     st.run(dev["k"], dev["v"], dev["idx_k"], dev["slot"], dev["q"], dev["idx_q"], dev["seq_lens"])
     ref = st.out.clone()
     host = {kk: vv.cpu() for kk, vv in dev.items()}
-    for zc in (True, False):
-        hs = step.HostDecodeStep(st, host, zero_copy=zc)
-        out = hs.run()
-        torch.cuda.synchronize()
-        assert st.dev_err.item() == 0
-        assert torch.equal(out, ref.cpu()), zc
+    for inputs in ("zero", "copy"):
+        for output in ("zero", "copy"):
+            hs = step.HostDecodeStep(st, host, inputs=inputs, output=output)
+            out = hs.run()
+            torch.cuda.synchronize()
+            assert st.dev_err.item() == 0
+            assert torch.equal(out, ref.cpu()), (inputs, output)
 
 
 @pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2"])
