@@ -418,10 +418,7 @@ bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_page
 // that kernel's occupancy and a 4-deep ring
 void plan_mx_tc(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
-#ifndef BSP_MXTC_START_X10
-#define BSP_MXTC_START_X10 0
-#endif
-  const double start_blocks = BSP_MXTC_START_X10 ? BSP_MXTC_START_X10 / 10.0 : kStartBytes / kMxField;
+  const double start_blocks = kStartBytes / kMxField;
   const int64_t resident = static_cast<int64_t>(index_score_mx_tc_occupancy()) * num_sms;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {
@@ -441,10 +438,7 @@ cudaError_t launch_index_score(IndexScoreParams p, int num_sms, cudaStream_t s) 
   if (p.num_rows == 0 || p.max_pages == 0) return cudaSuccess;
   p.num_groups = (p.num_tokens + p.q_group - 1) / p.q_group;
   const int64_t max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
-#ifndef BSP_IDX_MX_TC
-#define BSP_IDX_MX_TC 1
-#endif
-  if (BSP_IDX_MX_TC && !p.sel_counters && index_score_mx_tc_supported(p)) {
+  if (!p.sel_counters && index_score_mx_tc_supported(p)) {
     plan_mx_tc(p, max_blocks, num_sms);
     const int64_t cb = p.blocks_per_chunk;
     return launch_index_score_mx_tc(

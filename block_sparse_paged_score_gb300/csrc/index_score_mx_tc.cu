@@ -37,10 +37,7 @@ namespace bsp {
 
 namespace {
 
-#ifndef BSP_MXTC_STAGES
-#define BSP_MXTC_STAGES 3
-#endif
-constexpr int kStages = BSP_MXTC_STAGES;
+constexpr int kStages = 3;  // 53 KB of shared memory: 4 CTAs per SM
 constexpr int kScaleSlots = kStages + 2;  // a block's scales live until its epilogue is done
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (1 + kEpiWarps);
