@@ -6,7 +6,8 @@
 //
 // Rows of up to 128 pages: one warp per row (topk_warp_kernel).  Up to 8192:
 // one CTA of 256 threads per row with the keys in registers
-// (topk_cta_kernel).  Longer rows: one CTA of 512 threads per row with the
+// (topk_cta_kernel); when there are fewer rows than twice the SMs, one CTA of
+// 512 or 1024 threads per row instead, up to 32768 pages.  Longer rows: one CTA of 512 threads per row with the
 // keys in shared memory (topk_select_kernel).  Scores become order-preserving
 // uint32 keys (-0 folded onto +0).  A most-significant-digit
 // radix select (four 8-bit passes, shared-memory histograms, one warp scans
@@ -310,19 +311,19 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
 // go first.  Every CTA still waits before it exits.
 constexpr int kCtaThreads = 256;
 
-template <int KPT>
-__global__ void __launch_bounds__(kCtaThreads) topk_cta_kernel(TopkParams p) {
+template <int KPT, int NT = kCtaThreads>
+__global__ void __launch_bounds__(NT) topk_cta_kernel(TopkParams p) {
   __shared__ int s_hist[4][256];
-  __shared__ int s_warp[kCtaThreads / 32];
+  __shared__ int s_warp[NT / 32];
   __shared__ uint32_t s_digit;
   __shared__ int s_above;
-  for (int i = threadIdx.x; i < 4 * 256; i += kCtaThreads) (&s_hist[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < 4 * 256; i += NT) (&s_hist[0][0])[i] = 0;
   const bool in_step = p.rows_per_seq > 0;
   if (!in_step) {
     pdl_wait();  // scores (and the row lengths) come from earlier kernels
     pdl_trigger();
   }
-  select_row_cta<KPT, kCtaThreads, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
+  select_row_cta<KPT, NT, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
 }
 
 // 128-token blocks as the unit of selection (pages_per_block = 8).  One CTA
@@ -457,9 +458,21 @@ cudaError_t launch_blocks(const TopkParams& p, cudaStream_t s) {
   return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
-template <int KPT>
+int device_sms_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+                                                   cudaSuccess)
+      n = v;
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int KPT, int NT = kCtaThreads>
 cudaError_t launch_cta(const TopkParams& p, cudaStream_t s) {
-  const cudaError_t e = launch_kernel(topk_cta_kernel<KPT>, dim3(p.num_rows), dim3(kCtaThreads), 0, s, 0, p);
+  const cudaError_t e = launch_kernel(topk_cta_kernel<KPT, NT>, dim3(p.num_rows), dim3(NT), 0, s, 0, p);
   return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
@@ -486,6 +499,17 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.max_pages <= 512 && BSP_TOPK_WARP_MAX >= 512) return launch_warp<16>(p, s);
   if (p.max_pages <= 1024 && BSP_TOPK_WARP_MAX >= 1024) return launch_warp<32>(p, s);
   if (p.max_pages <= 2048 && BSP_TOPK_WARP_MAX >= 2048) return launch_warp<64>(p, s);
+  // Few long rows leave most SMs idle with one 256-thread CTA a row: give
+  // each row a 512- or 1024-thread CTA instead (fewer keys per thread)
+  if (p.max_pages > kCtaThreads && p.max_pages <= 32 * 1024 &&
+      p.num_rows < 2 * device_sms_count()) {
+    if (p.max_pages <= 512) return launch_cta<1, 512>(p, s);
+    if (p.max_pages <= 2 * 1024) return launch_cta<2, 1024>(p, s);
+    if (p.max_pages <= 4 * 1024) return launch_cta<4, 1024>(p, s);
+    if (p.max_pages <= 8 * 1024) return launch_cta<8, 1024>(p, s);
+    if (p.max_pages <= 16 * 1024) return launch_cta<16, 1024>(p, s);
+    return launch_cta<32, 1024>(p, s);
+  }
   if (p.max_pages <= 1 * kCtaThreads) return launch_cta<1>(p, s);
   if (p.max_pages <= 2 * kCtaThreads) return launch_cta<2>(p, s);
   if (p.max_pages <= 4 * kCtaThreads) return launch_cta<4>(p, s);
