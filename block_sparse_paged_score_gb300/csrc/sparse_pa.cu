@@ -45,45 +45,24 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// fp8 -> f16 of the K/V pages: the integer bit move (value * 2^-8) or the
-// hardware cvt (value * 1); the power of two is folded into the scales
-#ifndef BSP_PA_E4M3_CVT
-#define BSP_PA_E4M3_CVT 1
-#endif
-constexpr float kE4m3Fold = BSP_PA_E4M3_CVT ? 1.f : 256.f;
+// fp8 -> f16 of the K/V pages with the hardware cvt (exact)
 __device__ __forceinline__ void kv_e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  if (BSP_PA_E4M3_CVT)
-    e4m3x4_to_f16x2_cvt(w, lo, hi);
-  else
-    e4m3x4_to_f16x2_scaled(w, lo, hi);
+  e4m3x4_to_f16x2_cvt(w, lo, hi);
 }
 constexpr float kRescaleLog2 = 8.f;
 
 template <int KV>
 struct PaFmt;
-// pages in flight per warp (fp8) and the split plan's target of resident
-// CTAs per SM; compile-time so that they can be tuned by measurement
-#ifndef BSP_PA_FP8_RING
-#define BSP_PA_FP8_RING 3
-#endif
-// resident CTAs per SM the per-row split plan targets (0: the kernel's
-// occupancy as the CUDA runtime reports it)
-#ifndef BSP_PA_CTAS_PER_SM
-#define BSP_PA_CTAS_PER_SM 0
-#endif
 constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 
-// kMinCtas: resident CTAs per SM the per-row kernel is compiled for (its
-// register budget); fp8 fits four (16 warps per SM) with a 3-page ring
-#ifndef BSP_PA_FP8_MIN_CTAS
-#define BSP_PA_FP8_MIN_CTAS 4
-#endif
-#ifndef BSP_PA_MX_MIN_CTAS
-#define BSP_PA_MX_MIN_CTAS 2
-#endif
+// Per format: kRing, the default pages in flight per warp (the plan deepens
+// it up to kRingMax while the grid fits one wave); kSlot, the bytes of one
+// page of K and V; kDeq, the bf16 page a warp dequantises MXFP4 into;
+// kMinCtas, the resident CTAs per SM the kernel is compiled for (its register
+// budget: fp8 fits four, 16 warps per SM, with a 3-page ring).  All measured.
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
-  static constexpr int kRing = BSP_PA_FP8_RING, kRingMax = 6, kSlot = 4096, kDeq = 0, kMinCtas = BSP_PA_FP8_MIN_CTAS;
+  static constexpr int kRing = 3, kRingMax = 6, kSlot = 4096, kDeq = 0, kMinCtas = 4;
 };
 template <>
 struct PaFmt<BSP_BF16> {
@@ -92,7 +71,7 @@ struct PaFmt<BSP_BF16> {
 template <>
 struct PaFmt<BSP_MXFP4> {
   // K data 1024 | K scales 64 | V data 1024 | V scales 64
-  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = BSP_PA_MX_MIN_CTAS;
+  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
 };
 
 // shared memory: the rings (and MXFP4 dequant pages) during the page loop,
@@ -737,8 +716,8 @@ cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
     const cudaError_t e = configure_kv<KV>();
     if (e != cudaSuccess) return e;
   }
-  const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale * kE4m3Fold : 1.f;
-  const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale * kE4m3Fold : 1.f;
+  const float kfold = KV == BSP_FP8_E4M3 ? p.k_scale : 1.f;
+  const float vfold = KV == BSP_FP8_E4M3 ? p.v_scale : 1.f;
   const float qk_scale = p.sm_scale * kfold * kLog2e;
   const int64_t ctas = static_cast<int64_t>(p.num_rows) * p.nsplit;
   const cudaError_t e = launch_kernel(sparse_pa_kernel<KV>, dim3(static_cast<unsigned>(ctas)), dim3(128),
@@ -772,7 +751,7 @@ PaPlan plan_kv(int32_t num_rows, int32_t k_pages, int num_sms) {
   // up to 8 splits form one cluster and merge on chip, more (very few rows)
   // merge through the workspace
   const int base_ring = PaFmt<KV>::kRing;
-  const int64_t per_sm = BSP_PA_CTAS_PER_SM > 0 ? BSP_PA_CTAS_PER_SM : occupancy_kv<KV>(base_ring);
+  const int64_t per_sm = occupancy_kv<KV>(base_ring);
   int64_t ns = per_sm * num_sms / rows;
   const int64_t max_ns = std::min<int64_t>(64, (k_pages + 3) / 4);
   ns = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);

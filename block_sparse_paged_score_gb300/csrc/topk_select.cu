@@ -7,8 +7,9 @@
 // Rows of up to 128 pages: one warp per row (topk_warp_kernel).  Up to 8192:
 // one CTA of 256 threads per row with the keys in registers
 // (topk_cta_kernel); when there are fewer rows than twice the SMs, one CTA of
-// 512 or 1024 threads per row instead, up to 32768 pages.  Longer rows: one CTA of 512 threads per row with the
-// keys in shared memory (topk_select_kernel).  Scores become order-preserving
+// 512 or 1024 threads per row instead, up to 32768 pages.  Longer rows: one
+// CTA of 512 threads per row with the keys in shared memory
+// (topk_select_kernel).  Scores become order-preserving
 // uint32 keys (-0 folded onto +0).  A most-significant-digit
 // radix select (four 8-bit passes, shared-memory histograms, one warp scans
 // the 256 bins) finds the k'-th largest key tau and how many keys equal to
@@ -299,11 +300,6 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
   }
 }
 
-// the longest rows (pages) the one-warp-per-row kernel takes
-#ifndef BSP_TOPK_WARP_MAX
-#define BSP_TOPK_WARP_MAX 128
-#endif
-
 // One CTA of 256 threads per row of up to 256*KPT pages (select_row_cta).
 // Inside the decode step (rows_per_seq > 0) the row lengths come from the
 // step's first kernel, done before the scorer started: only the scores need
@@ -495,10 +491,7 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
     if (nblk <= 16 * kCtaThreads) return launch_blocks<16>(p, s);
     return launch_blocks<32>(p, s);  // max_pages <= 65536
   }
-  if (p.max_pages <= 128 && BSP_TOPK_WARP_MAX >= 128) return launch_warp<4>(p, s);
-  if (p.max_pages <= 512 && BSP_TOPK_WARP_MAX >= 512) return launch_warp<16>(p, s);
-  if (p.max_pages <= 1024 && BSP_TOPK_WARP_MAX >= 1024) return launch_warp<32>(p, s);
-  if (p.max_pages <= 2048 && BSP_TOPK_WARP_MAX >= 2048) return launch_warp<64>(p, s);
+  if (p.max_pages <= 128) return launch_warp<4>(p, s);  // one warp a row (longer rows measured slower)
   // Few long rows leave most SMs idle with one 256-thread CTA a row: give
   // each row a 512- or 1024-thread CTA instead (fewer keys per thread)
   if (p.max_pages > kCtaThreads && p.max_pages <= 32 * 1024 &&
