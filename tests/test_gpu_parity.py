@@ -459,3 +459,30 @@ def test_decode_step_selection_in_scorer(bsp, name):
             assert torch.equal(getattr(a, x), getattr(b, x)), x
         assert int(b.sel_counters.abs().sum().item()) == 0
     assert launches == [3, 3]  # prep, scorer with selection, attention
+
+
+@pytest.mark.parametrize("name", ["fp8", "mx"])
+def test_decode_step_in_a_cuda_graph(bsp, name):
+    """The library allocates nothing and never synchronises, so a decode step
+    captures into a CUDA graph (its kernels' programmatic launches included);
+    replaying the graph gives the direct call's result bit for bit."""
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides(name)
+    st = step.DecodeStep(w, g.kv, g.idx, g.block_table)
+    k, v, ik, slot = w.step_tokens()
+    args = (g.t(k), g.t(v), g.t(ik), g.t(slot), g.q_bf16, g.idx_q_bf16, g.t(w.decode_lens))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        st.run(*args, stream=s)
+    torch.cuda.synchronize()
+    ref = st.out.clone()
+    st.out.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        st.run(*args, stream=s)
+    for _ in range(2):
+        st.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert st.dev_err.item() == 0
+        assert torch.equal(st.out, ref)
