@@ -5,7 +5,8 @@ Stage by stage, each GPU stage gets inputs that both sides computed
 identically or that the oracle computed (never the other way round):
   write      byte-exact cache bytes;
   scores     |gpu - oracle| <= 2e-5 * sum_d |q_d k_d| (fp32 accumulation of
-             128 exact products, see DESIGN.md), -inf pattern identical;
+             128 exact products, at most (128 + 1) * 2^-23 of sum |qk|),
+             -inf pattern identical;
   top-k      bit-exact when the GPU selector is fed the oracle's scores;
   attention  max-abs 1e-2 and relative-L2 5e-3 (bf16 out) when the GPU
              attention is fed the oracle's sparse table.
