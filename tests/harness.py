@@ -25,6 +25,11 @@ MINI = {
                hkv=1, group=16, k_pages=16, q_len=1, decode_lens=[1, 16, 33, 260, 700, 1300]),
     "mx_bf16q": dict(name="mini-mx-bf16q", seed=16, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.BF16,
                      idx_q_dtype=W.BF16, hkv=2, group=4, k_pages=8, q_len=2, decode_lens=[5, 300, 777]),
+    # the longest decode query (q_len 8): full 8-row groups in every scorer
+    "fp8_q8": dict(name="mini-fp8-q8", seed=18, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
+                   hkv=1, group=16, k_pages=16, q_len=8, decode_lens=[3, 8, 9, 200, 1100]),
+    "mx_q8": dict(name="mini-mx-q8", seed=19, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8, idx_q_dtype=W.FP8,
+                  hkv=1, group=16, k_pages=16, q_len=8, decode_lens=[5, 8, 130, 1300]),
     "mixed": dict(name="mini-mixed", seed=17, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
                   hkv=1, group=16, k_pages=16, q_len=1, decode_lens=[40, 900],
                   prefill_chunks=[(384, 200), (700, 300)], pad_seqs=1, pad_q_len=4),
