@@ -59,7 +59,9 @@ constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 // it up to kRingMax while the grid fits one wave); kSlot, the bytes of one
 // page of K and V; kDeq, the bf16 page a warp dequantises MXFP4 into;
 // kMinCtas, the resident CTAs per SM the kernel is compiled for (its register
-// budget: fp8 fits four, 16 warps per SM, with a 3-page ring).  All measured.
+// budget: fp8 fits four, 16 warps per SM, with a 3-page ring; MXFP4 fits
+// four with a 2-page ring, the most its dequant pages leave room for).  All
+// measured.
 template <>
 struct PaFmt<BSP_FP8_E4M3> {
   static constexpr int kRing = 3, kRingMax = 6, kSlot = 4096, kDeq = 0, kMinCtas = 4;
@@ -71,7 +73,7 @@ struct PaFmt<BSP_BF16> {
 template <>
 struct PaFmt<BSP_MXFP4> {
   // K data 1024 | K scales 64 | V data 1024 | V scales 64
-  static constexpr int kRing = 3, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = 2;
+  static constexpr int kRing = 2, kRingMax = 6, kSlot = 2176, kDeq = 8192, kMinCtas = 4;
 };
 
 // shared memory: the rings (and MXFP4 dequant pages) during the page loop,
@@ -93,28 +95,14 @@ __host__ __device__ constexpr int pa_smem_bytes(int ring) {
   return pa_bar_offset<KV>(ring) + kQFragBytes + 4 * ring * 8;
 }
 
-// n (2 or 4) consecutive query elements starting at element `off`
-// (8-byte or 4-byte aligned for bf16, 4- or 2-byte for e4m3)
-__device__ __forceinline__ void load_q_vals(const void* q, int q_dtype, int64_t off, int n, float* v) {
-  if (q_dtype == BSP_BF16) {
-    const uint16_t* p = static_cast<const uint16_t*>(q) + off;
-    if (n == 4) {
-      const uint2 w = *reinterpret_cast<const uint2*>(p);
-      v[0] = bf16_bits_to_float(w.x & 0xFFFF), v[1] = bf16_bits_to_float(w.x >> 16);
-      v[2] = bf16_bits_to_float(w.y & 0xFFFF), v[3] = bf16_bits_to_float(w.y >> 16);
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-      v[0] = bf16_bits_to_float(w & 0xFFFF), v[1] = bf16_bits_to_float(w >> 16);
-    }
-  } else {
-    const uint8_t* p = static_cast<const uint8_t*>(q) + off;
-    const uint32_t w = n == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
-    for (int i = 0; i < n; ++i) v[i] = e4m3_to_float(w >> (8 * i));
-  }
-}
+// Row of dim d in a dequantised V page: the 16-byte rows (8 tokens of one
+// dim) are rotated within each group of 8 by d/8, so that the dequant's
+// stores (lane L writes dims 4L..4L+3) spread over all 32 banks; a
+// ldmatrix of 8 consecutive dims still reads one 128-byte block.
+__device__ __forceinline__ int mx_vrow(int d) { return (d & ~7) | ((d + (d >> 3)) & 7); }
 
 // dequantise one MXFP4 page (K and V, 16 tokens) into the bf16 page layout
-// K [d/8][16 t][8], V [t/8][128 d][8]
+// K [d/8][16 t][8], V [t/8][128 rows][8] (dim d at row mx_vrow(d))
 __device__ __forceinline__ void mx_page_to_bf16(const uint8_t* slot, uint8_t* dq, int lane) {
   {  // K: lane = (token, half of the dims)
     const int tk = lane >> 1, hf = lane & 1;
@@ -156,7 +144,7 @@ __device__ __forceinline__ void mx_page_to_bf16(const uint8_t* slot, uint8_t* dq
         w.y = pack_bf16x2(v[2][i], v[3][i]);
         w.z = pack_bf16x2(v[4][i], v[5][i]);
         w.w = pack_bf16x2(v[6][i], v[7][i]);
-        *reinterpret_cast<uint4*>(dq + 4096 + th * 2048 + (4 * lane + i) * 16) = w;
+        *reinterpret_cast<uint4*>(dq + 4096 + th * 2048 + mx_vrow(4 * lane + i) * 16) = w;
       }
     }
   }
@@ -389,8 +377,8 @@ __device__ __forceinline__ void pa_page(PaState& a, uint32_t qs, uint32_t kaddr,
 #pragma unroll
     for (int q8 = 0; q8 < 8; ++q8) {
       uint32_t r[4];
-      ldsm_x4(r[0], r[1], r[2], r[3],
-              vaddr + ((lane >> 3) & 1) * 2048 + (8 * (2 * q8 + (lane >> 4)) + (lane & 7)) * 16);
+      const int d = 8 * (2 * q8 + (lane >> 4)) + (lane & 7);
+      ldsm_x4(r[0], r[1], r[2], r[3], vaddr + ((lane >> 3) & 1) * 2048 + (KV == BSP_MXFP4 ? mx_vrow(d) : d) * 16);
       mma_bf16(a.o[2 * q8], pa0, pa1, pa2, pa3, r[0], r[1]);
       mma_bf16(a.o[2 * q8], lo0, lo1, lo2, lo3, r[0], r[1]);
       mma_bf16(a.o[2 * q8 + 1], pa0, pa1, pa2, pa3, r[2], r[3]);
