@@ -20,9 +20,12 @@ _lib = None
 
 
 def lib():
+    """The oracle library: the built ``liboracle.so``, or the library named by
+    ``BSP_ORACLE_LIB`` (the planted-mistake test loads variants of the oracle
+    this way)."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = os.environ.get("BSP_ORACLE_LIB") or _build.build()
         _lib = C.CDLL(path)
         _declare(_lib)
     return _lib
