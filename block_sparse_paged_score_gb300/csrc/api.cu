@@ -16,18 +16,16 @@ namespace {
 std::atomic<int32_t> g_last_cuda_error{0};
 std::atomic<int64_t> g_launches{0};
 
-constexpr int kMaxDevices = 64;
-int g_sms[kMaxDevices] = {0};
+std::atomic<int> g_sms[kMaxDevices];
 
 int device_sms() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (!g_sms[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    g_sms[dev] = n;
-  }
-  return g_sms[dev];
+  return cached_per_device(g_sms, [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || n <= 0)
+      n = 148;
+    return n;
+  });
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }

@@ -329,31 +329,29 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
   if constexpr (SEL > 0) select_unit<SEL>(p, s_row, ntok, smem);
 }
 
-// the dynamic shared-memory opt-in (once per process; per function)
+// the dynamic shared-memory opt-in (once per device; per function)
 template <int KEY, int SEL>
 cudaError_t configure_key() {
-  static bool configured = false;
-  if (configured) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(index_score_kernel<KEY, SEL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes<KEY>(KeyFmt<KEY>::kStages));
-  if (e == cudaSuccess) configured = true;
-  return e;
+  static std::atomic<uint64_t> done{0};
+  return once_per_device(done, [] {
+    return cudaFuncSetAttribute(index_score_kernel<KEY, SEL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes<KEY>(KeyFmt<KEY>::kStages));
+  });
 }
 
 // resident CTAs per SM with a ring of `stages` fields (queried once per depth;
 // a failed query assumes 1)
 template <int KEY, int SEL>
 int occupancy_key(int stages) {
-  static int cache[KeyFmt<KEY>::kStages + 1] = {};
-  if (!cache[stages]) {
+  static std::atomic<int> cache[KeyFmt<KEY>::kStages + 1][kMaxDevices];
+  return cached_per_device(cache[stages], [stages] {
     int n = 0;
     cudaError_t e = configure_key<KEY, SEL>();
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, index_score_kernel<KEY, SEL>, 128,
                                                         smem_bytes<KEY>(stages));
-    cache[stages] = (e == cudaSuccess && n > 0) ? n : 1;
-  }
-  return cache[stages];
+    return (e == cudaSuccess && n > 0) ? n : 1;
+  });
 }
 
 // Blocks per CTA (cb) and ring depth.  Each CTA pays a fixed start (row

@@ -262,17 +262,16 @@ bool index_score_mx_tc_supported(const IndexScoreParams& p) {
 }
 
 int index_score_mx_tc_occupancy() {
-  static int n = 0;
-  if (!n) {
+  static std::atomic<int> table[kMaxDevices];
+  return cached_per_device(table, [] {
     int v = 0;
     if (cudaFuncSetAttribute(index_score_mx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, index_score_mx_tc_kernel, kThreads, kSmemBytes) !=
             cudaSuccess)
       v = 1;
-    n = std::max(1, std::min(v, 512 / (2 * kAccCols)));  // TMEM: 128 columns a CTA
-  }
-  return n;
+    return std::max(1, std::min(v, 512 / (2 * kAccCols)));  // TMEM: 128 columns a CTA
+  });
 }
 
 cudaError_t launch_index_score_mx_tc(const IndexScoreParams& p, dim3 grid, cudaStream_t s) {

@@ -292,12 +292,12 @@ cudaError_t launch_index_score_prefill_mx(const PrefillScoreParams& p, cudaStrea
   if ((reinterpret_cast<uintptr_t>(p.idx_base) & 31) || p.block_stride % 64) return cudaErrorNotSupported;
   if (!make_map_u8(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map_u4(&tk, p.idx_base, key_rows, 64))
     return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(index_score_prefill_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<uint64_t> configured{0};
+  {
+    const cudaError_t e = once_per_device(configured, [] {
+      return cudaFuncSetAttribute(index_score_prefill_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
   const dim3 grid(static_cast<unsigned>(p.max_tiles),

@@ -285,12 +285,12 @@ cudaError_t launch_index_score_prefill(const PrefillScoreParams& p, cudaStream_t
   const uint64_t key_rows = static_cast<uint64_t>(p.num_blocks) * (p.block_stride / 128);
   if (!make_map_u8(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map_u8(&tk, p.idx_base, key_rows))
     return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(index_score_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<uint64_t> configured{0};
+  {
+    const cudaError_t e = once_per_device(configured, [] {
+      return cudaFuncSetAttribute(index_score_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int max_blocks = (p.max_pages + kPagesPerSide - 1) / kPagesPerSide;
   const dim3 grid(static_cast<unsigned>(p.max_tiles),

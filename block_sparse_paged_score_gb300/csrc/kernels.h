@@ -6,7 +6,43 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace bsp {
+
+// Per-device host state.  A kernel's dynamic shared-memory opt-in and the
+// occupancy it allows belong to the current device's context, so they are
+// kept per device (one process may drive several GPUs) and in atomics
+// (several host threads may call the library at once; every writer stores
+// the same value).
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = -1;
+  return (cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices) ? d : -1;
+}
+// set() once per device; `done` holds one bit per device that has it (a
+// device outside the table runs set() every time)
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, F set) {
+  const int d = current_device();
+  const uint64_t bit = d >= 0 ? (uint64_t{1} << d) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+// a positive value per device, computed by get() the first time
+template <typename F>
+inline int cached_per_device(std::atomic<int> (&table)[kMaxDevices], F get) {
+  const int d = current_device();
+  if (d < 0) return get();
+  int v = table[d].load(std::memory_order_acquire);
+  if (!v) {
+    v = get();
+    table[d].store(v, std::memory_order_release);
+  }
+  return v;
+}
 
 // Every kernel of the library goes through this launch: programmatic stream
 // serialization (the kernel may be scheduled while the previous kernel on the

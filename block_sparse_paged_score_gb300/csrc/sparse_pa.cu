@@ -686,15 +686,14 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
   if (tid == 0) counters[row] = 0;  // ready for the next call
 }
 
-// the dynamic shared-memory opt-in of a kernel: its largest ring (once per process)
+// the dynamic shared-memory opt-in of a kernel: its largest ring (once per device)
 template <int KV>
 cudaError_t configure_kv() {
-  static bool configured = false;
-  if (configured) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             pa_smem_bytes<KV>(PaFmt<KV>::kRingMax));
-  if (e == cudaSuccess) configured = true;
-  return e;
+  static std::atomic<uint64_t> done{0};
+  return once_per_device(done, [] {
+    return cudaFuncSetAttribute(sparse_pa_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                pa_smem_bytes<KV>(PaFmt<KV>::kRingMax));
+  });
 }
 
 template <int KV>
@@ -719,15 +718,14 @@ cudaError_t launch_kv(const SparsePaParams& p, cudaStream_t s, int* launches) {
 // warp (queried once per format and depth; a failed query assumes 1)
 template <int KV>
 int occupancy_kv(int ring) {
-  static int cache[PaFmt<KV>::kRingMax + 1] = {};
-  if (!cache[ring]) {
+  static std::atomic<int> cache[PaFmt<KV>::kRingMax + 1][kMaxDevices];
+  return cached_per_device(cache[ring], [ring] {
     int n = 0;
     cudaError_t e = configure_kv<KV>();
     if (e == cudaSuccess)
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sparse_pa_kernel<KV>, 128, pa_smem_bytes<KV>(ring));
-    cache[ring] = (e == cudaSuccess && n > 0) ? n : 1;
-  }
-  return cache[ring];
+    return (e == cudaSuccess && n > 0) ? n : 1;
+  });
 }
 
 template <int KV>

@@ -455,15 +455,14 @@ cudaError_t launch_blocks(const TopkParams& p, cudaStream_t s) {
 }
 
 int device_sms_count() {
-  static int n = 0;
-  if (!n) {
+  static std::atomic<int> table[kMaxDevices];
+  return cached_per_device(table, [] {
     int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-                                                   cudaSuccess)
-      n = v;
-    if (n <= 0) n = 1;
-  }
-  return n;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      v = 0;
+    return v > 0 ? v : 1;
+  });
 }
 
 template <int KPT, int NT = kCtaThreads>
@@ -511,12 +510,12 @@ cudaError_t launch_topk_select(const TopkParams& p, cudaStream_t s) {
   if (p.max_pages <= 32 * kCtaThreads) return launch_cta<32>(p, s);
   const int cand = p.max_pages < kSmemKeys ? p.max_pages : kSmemKeys;
   const size_t bytes = static_cast<size_t>(cand) * 4;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
+  static std::atomic<uint64_t> configured{0};
+  {
+    const cudaError_t e = once_per_device(configured, [] {
+      return cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKeys * 4);
+    });
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const cudaError_t e = launch_kernel(topk_select_kernel, dim3(p.num_rows), dim3(kThreads), bytes, s, 0, p);
   return e != cudaSuccess ? e : cudaPeekAtLastError();
