@@ -1,6 +1,6 @@
 """Planted mistakes: the pins are not the oracle restated.
 
-Each case copies the oracle's C sources to a temporary folder, plants one
+Each case copies the oracle's C sources to a scratch folder, plants one
 plausible mistake in the copy (a wrong bias, sign bit or rounding rule, a
 dropped scale, a transposed layout, an off-by-one length, a broken tie rule, a
 swapped operand), builds that variant and runs the oracle's pin tests against
@@ -91,7 +91,7 @@ MISTAKES = {
 def _build_variant(name, folder):
     fname, old, new = MISTAKES[name]
     d = os.path.join(folder, "v%02d" % sorted(MISTAKES).index(name))
-    shutil.copytree(ORACLE, d, ignore=shutil.ignore_patterns("*.so", "*.tmp", "__pycache__"))
+    shutil.copytree(ORACLE, d, ignore=shutil.ignore_patterns("*.so", "*.tmp", "__pycache__", "_planted"))
     path = os.path.join(d, fname)
     src = open(path).read()
     assert src.count(old) == 1, (name, "the planted site must occur once")
@@ -116,7 +116,9 @@ def _run_pins(lib):
 
 @pytest.fixture(scope="module")
 def outcomes():
-    folder = tempfile.mkdtemp(prefix="oracle_planted_")
+    scratch = os.path.join(ORACLE, "_planted")  # git-ignored; removed afterwards
+    os.makedirs(scratch, exist_ok=True)
+    folder = tempfile.mkdtemp(prefix="run_", dir=scratch)
     try:
         names = sorted(MISTAKES)
         with cf.ThreadPoolExecutor(max(2, min(8, os.cpu_count() or 2))) as ex:
@@ -125,6 +127,10 @@ def outcomes():
         yield res
     finally:
         shutil.rmtree(folder, ignore_errors=True)
+        try:
+            os.rmdir(scratch)  # only when no other run is using it
+        except OSError:
+            pass
 
 
 @pytest.mark.parametrize("name", sorted(MISTAKES))
