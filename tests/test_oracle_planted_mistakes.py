@@ -43,6 +43,8 @@ MISTAKES = {
     "e8m0 bias 128": ("codecs.c", "ldexp(1.0, (int)b - 127)", "ldexp(1.0, (int)b - 128)"),
     "bf16 ties away from zero": ("codecs.c", "(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
     "MX shared exponent off by one": ("codecs.c", "e = (ex - 1) - 2;", "e = (ex - 1) - 1;"),
+    "all-zero MX group with scale 1": ("codecs.c", "    e = -127;\n", "    e = 0;\n"),
+    "e4m3 subnormals a binade low": ("codecs.c", "v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
     # layout and writer
     "K page token-major": ("layout.c", "elem = (int64_t)(d / x) * ORC_PAGE * x + (int64_t)t * x + d % x;",
                            "elem = (int64_t)t * ORC_DIM + d;"),
@@ -60,6 +62,9 @@ MISTAKES = {
     # row lengths and scores
     "decode length off by one": ("score.c", "int64_t L = (int64_t)seq_lens[s] - (q_len - 1 - j);",
                                  "int64_t L = (int64_t)seq_lens[s] - (q_len - j);"),
+    "pad rows not clamped": ("score.c", "int64_t L = (int64_t)seq_lens[s] - (q_len - 1 - j);\n      if (L < 0) L = 0;",
+                             "int64_t L = (int64_t)seq_lens[s] - (q_len - 1 - j);"),
+    "index head of a row from its token": ("score.c", "int h = r % Hidx;", "int h = (r / Hidx) % Hidx;"),
     "prefill length without the +1": ("score.c", "int64_t L = (int64_t)query_abs_pos[i] + 1;",
                                       "int64_t L = (int64_t)query_abs_pos[i];"),
     "fp8 index key scale dropped": ("score.c", "float kd = (float)orc_e4m3_decode(field[o * 128 + d]) * s;",
@@ -76,7 +81,18 @@ MISTAKES = {
                                      "block_table[(int64_t)row_seq[r] * bt_stride + p / ORC_PAGE];"),
     "block score of its first page, not the max": ("topk.c", "if (sr[p] > best) best = sr[p];", "(void)best;"),
     "MX scale bytes of a token swapped": ("write.c", "field[8192 + t * 4 + g] = sb;", "field[8192 + t * 4 + (g ^ 1)] = sb;"),
+    "partial tail page counted as 16 tokens": ("topk.c",
+                                               "      ti[m] = p;\n      bt[m] = (int32_t)(id_rule == 0 ? block * 16 + p % ORC_PAGES_PER_SIDE\n"
+                                               "                                     : block * ORC_PAGES_PER_SIDE + p % ORC_PAGES_PER_SIDE);\n"
+                                               "      ctx += (p == n - 1) ? tail_len : ORC_PAGE;",
+                                               "      ti[m] = p;\n      bt[m] = (int32_t)(id_rule == 0 ? block * 16 + p % ORC_PAGES_PER_SIDE\n"
+                                               "                                     : block * ORC_PAGES_PER_SIDE + p % ORC_PAGES_PER_SIDE);\n"
+                                               "      ctx += ORC_PAGE;"),
     # attention
+    "every token read as its page's first": ("attention.c", "int t = (int)(m % ORC_PAGE);", "int t = 0;"),
+    "KV head of a sparse row from its token": ("attention.c",
+                                               "    int h = r % Hkv;\n    int64_t n = sparse_ctx[r] < 0 ? 0 : sparse_ctx[r];",
+                                               "    int h = (r / Hkv) % Hkv;\n    int64_t n = sparse_ctx[r] < 0 ? 0 : sparse_ctx[r];"),
     "softmax scale dropped": ("attention.c", "z[m] = (double)sm_scale * dot;", "z[m] = dot;"),
     "k and v scales swapped": ("attention.c", "(side ? v_scale : k_scale)", "(side ? k_scale : v_scale)"),
     "MX V read from the K field": ("attention.c", "kv + orc_mx_field_offset(Hkv, block, side, h);",
