@@ -30,7 +30,6 @@ weak scaling, no collective on the data path.
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

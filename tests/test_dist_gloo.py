@@ -5,7 +5,6 @@ multi-GPU logic."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

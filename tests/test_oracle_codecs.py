@@ -5,7 +5,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 import torch
 
 import oracle as O
