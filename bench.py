@@ -253,11 +253,16 @@ def oracle_sample(w, seconds, blocks=False):
     return one if n == 1 else OracleStep(w, n, blocks)
 
 
-def cpu_oracle_rate(w, seconds=12.0, blocks=False):
+def cpu_oracle_rate(w, seconds=10.0, blocks=False):
+    """The oracle's rate on a sample of the workload: one warm-up pass, then
+    passes until about `seconds` have gone by (at least three)."""
     import oracle as O
     o = oracle_sample(w, seconds, blocks)
-    dt = o.run()
-    return o.tokens / dt, O.num_threads(), o.desc + ", one pass"
+    o.run()
+    times = []
+    while len(times) < 3 or sum(times) < seconds:
+        times.append(o.run())
+    return o.tokens * len(times) / sum(times), O.num_threads(), f"{o.desc}, mean of {len(times)} passes after a warm-up"
 
 
 # ---------------------------------------------------------------------------
