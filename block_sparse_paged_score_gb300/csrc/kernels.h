@@ -48,9 +48,6 @@ inline int cached_per_device(std::atomic<int> (&table)[kMaxDevices], F get) {
 // serialization (the kernel may be scheduled while the previous kernel on the
 // stream drains; it waits on griddepcontrol before touching global memory)
 // and, for cluster > 1, a 1-D thread-block cluster of that size.
-#ifndef BSP_PDL
-#define BSP_PDL 1
-#endif
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                                  int cluster, Args... args) {
@@ -61,11 +58,9 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
-  if (BSP_PDL) {
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
   if (cluster > 1) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
