@@ -65,6 +65,9 @@ MISTAKES = {
     "pad rows not clamped": ("score.c", "int64_t L = (int64_t)seq_lens[s] - (q_len - 1 - j);\n      if (L < 0) L = 0;",
                              "int64_t L = (int64_t)seq_lens[s] - (q_len - 1 - j);"),
     "index head of a row from its token": ("score.c", "int h = r % Hidx;", "int h = (r / Hidx) % Hidx;"),
+    "score magnitude without the absolute value": ("score.c", "adot += fabs(qv[d] * kv[d]);", "adot += qv[d] * kv[d];"),
+    "prefill pad rows not clamped": ("score.c", "int64_t L = (int64_t)query_abs_pos[i] + 1;\n    if (L < 0) L = 0;",
+                                     "int64_t L = (int64_t)query_abs_pos[i] + 1;"),
     "prefill length without the +1": ("score.c", "int64_t L = (int64_t)query_abs_pos[i] + 1;",
                                       "int64_t L = (int64_t)query_abs_pos[i];"),
     "fp8 index key scale dropped": ("score.c", "float kd = (float)orc_e4m3_decode(field[o * 128 + d]) * s;",
