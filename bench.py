@@ -5,9 +5,13 @@
 A step is one pass of the whole path over one batch: write the step's new
 tokens into the caches, cast the queries the writer emits as e4m3, row
 lengths, index scores, top-k with the emitted sparse table, attention (split-K
-+ merge).  The workload is one of the seeded synthetic configurations
-(default 2: 32 fp8 sequences of 4096..8192 tokens, 16 query heads per KV
-head, top-128 pages).
++ merge).  The workload is one of the seeded synthetic configurations:
+by default the largest decode batch that fits one GPU, 3: 128 fp8 sequences
+of 32768 tokens with 4 query tokens each (512 rows), the interleaved K/V
+layout, a block table that is a seeded random permutation, 16 query heads
+per KV head, top-128 pages (2048 tokens).  --config selects the others (1: the
+tiny bf16 case, 2: 32 fp8 sequences of 4096..8192 tokens, 4: MXFP4 64 x 128k,
+5/6: the chunked-prefill batch with an fp8 / MXFP4 index).
 
 Timing: every step is bracketed by CUDA events on the launching stream; an L2
 flush (a 256 MiB memset, twice the L2) runs before each step and is not
@@ -51,7 +55,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

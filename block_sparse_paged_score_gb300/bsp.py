@@ -78,6 +78,7 @@ SYMBOLS = {
     "bsp_sparse_pa_prefill": [C.POINTER(KvCacheDesc), C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                               C.c_int32, C.c_int32, C.c_float, C.c_void_p, C.c_void_p, C.c_void_p],
     "bsp_sparse_pa_decode_workspace_bytes": [C.c_int32, C.c_int32, C.c_int32],
+    "bsp_sparse_pa_decode_splits": [C.c_int32, C.c_int32, C.c_int32],
     "bsp_sparse_decode_step": [C.POINTER(DecodeStepArgs), C.c_void_p, C.c_void_p],
     "bsp_kv_block_bytes": [C.c_int32, C.c_int32],
     "bsp_index_field_bytes": [C.c_int32],
@@ -247,6 +248,12 @@ def topk_select(scores, row_seq, row_len, block_table, kv_dtype, k_pages, flags=
 
 def decode_workspace_bytes(num_rows, k_pages, group):
     return int(lib().bsp_sparse_pa_decode_workspace_bytes(num_rows, k_pages, group))
+
+
+def decode_splits(kv_dtype, num_rows, k_pages):
+    """CTAs per row of a decode attention call with these sizes (> 8: the
+    splits merge through the workspace)."""
+    return int(lib().bsp_sparse_pa_decode_splits(kv_dtype, num_rows, k_pages))
 
 
 def decode_workspace(num_rows, k_pages, group, device="cuda"):

@@ -338,19 +338,45 @@ size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, i
   return need;
 }
 
-static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
-                                   const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
-                                   int32_t k_pages, float sm_scale, void* out, void* ws, size_t ws_bytes,
-                                   int32_t* dev_err, bsp_stream_t stream, bool decode, bool q_early = false) {
+int32_t bsp_sparse_pa_decode_splits(int32_t kv_dtype, int32_t num_rows, int32_t k_pages) {
+  if (!valid_dtype(kv_dtype) || num_rows < 1 || k_pages < 1) return 0;
+  return sparse_pa_plan(kv_dtype, num_rows, k_pages, device_sms()).nsplit;
+}
+
+}  // extern "C"
+
+namespace bsp {
+
+bsp_status sparse_pa_check_args(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
+                                const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
+                                int32_t k_pages, const void* out) {
   bsp_status st = check_kv(kv);
   if (st != BSP_OK) return st;
   if (num_rows < 0 || k_pages < 1 || num_q_heads < 1) return BSP_ERR_INVALID_ARG;
   if (num_q_heads % kv->num_kv_heads || num_rows % kv->num_kv_heads) return BSP_ERR_INVALID_ARG;
-  const int32_t group = num_q_heads / kv->num_kv_heads;
-  if (!valid_group(group)) return BSP_ERR_UNSUPPORTED;
+  if (!valid_group(num_q_heads / kv->num_kv_heads)) return BSP_ERR_UNSUPPORTED;
   if (q_dtype != BSP_BF16 && q_dtype != BSP_FP8_E4M3) return BSP_ERR_UNSUPPORTED;
   if (num_rows == 0) return BSP_OK;
   if (!q || !sparse_bt || !sparse_ctx || !out || !al(out, 16) || !al(q, 16)) return BSP_ERR_INVALID_ARG;
+  return BSP_OK;
+}
+
+size_t sparse_pa_decode_ws_need(int32_t kv_dtype, int32_t num_rows, int32_t k_pages) {
+  if (num_rows <= 0 || k_pages <= 0) return 0;
+  return sparse_pa_ws_bytes(num_rows, sparse_pa_plan(kv_dtype, num_rows, k_pages, device_sms()));
+}
+
+}  // namespace bsp
+
+extern "C" {
+
+static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
+                                   const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
+                                   int32_t k_pages, float sm_scale, void* out, void* ws, size_t ws_bytes,
+                                   int32_t* dev_err, bsp_stream_t stream, bool decode, bool q_early = false) {
+  bsp_status st = sparse_pa_check_args(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, num_rows, k_pages, out);
+  if (st != BSP_OK || num_rows == 0) return st;
+  const int32_t group = num_q_heads / kv->num_kv_heads;
   SparsePaParams p{};
   p.kv_dtype = kv->dtype;
   p.hkv = kv->num_kv_heads;

@@ -8,6 +8,8 @@
 
 #include <atomic>
 
+#include "../../include/bsp.h"
+
 namespace bsp {
 
 // Per-device host state.  A kernel's dynamic shared-memory opt-in and the
@@ -191,6 +193,13 @@ size_t sparse_pa_ws_bytes(int32_t num_rows, const PaPlan& plan);
 // bytes of the per-row arrival counters at the start of the workspace
 size_t sparse_pa_counter_bytes(int32_t num_rows);
 cudaError_t launch_sparse_pa(const SparsePaParams& p, cudaStream_t s, int* launches);
+// the argument checks of the attention calls (the status they return before
+// anything is enqueued)
+bsp_status sparse_pa_check_args(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
+                                const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
+                                int32_t k_pages, const void* out);
+// workspace bytes the decode plan of this KV format needs on the current device
+size_t sparse_pa_decode_ws_need(int32_t kv_dtype, int32_t num_rows, int32_t k_pages);
 
 struct PrefillScoreParams {
   const uint8_t* idx_base;

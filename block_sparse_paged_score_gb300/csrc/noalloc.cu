@@ -13,11 +13,13 @@
 // that loads the library holds it until the process exits.  The first call
 // on a device looks up the array's device address with cudaGetSymbolAddress
 // (with that device current) and caches it; that first call should come
-// before any stream capture.  All calls share the array, which keeps the last
-// call's contents.  Its head holds the per-row arrival counters the split-K
-// merge needs at zero; every call clears them (an async memset on the
-// caller's stream, no allocation) before it launches.  Calls that overlap on
-// the GPU (concurrent streams) race on the array.
+// before any stream capture.  The cached address does not survive
+// cudaDeviceReset (the module, and with it the array, may then move).  All
+// calls share the array, which keeps the last call's contents.  When this
+// format's split-K plan needs a workspace, its head holds the per-row arrival
+// counters the merge needs at zero, and the call clears them (an async memset
+// on the caller's stream, no allocation) before it launches.  Calls that
+// overlap on the GPU (concurrent streams) race on the array.
 #include <mutex>
 
 #include "../../include/bsp.h"
@@ -40,7 +42,10 @@ extern "C" bsp_status bsp_sparse_pa_decode_noalloc(const bsp_kv_cache* kv, const
                                                    const int32_t* sparse_ctx, int32_t num_rows, int32_t k_pages,
                                                    float sm_scale, void* out, int32_t* dev_err,
                                                    bsp_stream_t stream) {
-  if (!kv || num_rows < 0 || k_pages < 1 || num_q_heads < 1 || kv->num_kv_heads < 1) return BSP_ERR_INVALID_ARG;
+  // the attention's own checks first: an invalid call enqueues nothing
+  const bsp_status st =
+      bsp::sparse_pa_check_args(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, num_rows, k_pages, out);
+  if (st != BSP_OK || num_rows == 0) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSP_ERR_CUDA;
   void* scratch = nullptr;
@@ -53,9 +58,12 @@ extern "C" bsp_status bsp_sparse_pa_decode_noalloc(const bsp_kv_cache* kv, const
     }
     scratch = g_scratch_addr[dev];
   }
-  const int32_t group = num_q_heads / kv->num_kv_heads;
-  if (bsp_sparse_pa_decode_workspace_bytes(num_rows, k_pages, group) > kScratchBytes) return BSP_ERR_WORKSPACE;
-  if (num_rows > 0 &&
+  // this format's plan: most plans merge on chip and need no workspace at
+  // all; a plan that does needs its counters zeroed, and both fit the
+  // scratch whenever `need` does (the counters sit at its head)
+  const size_t need = bsp::sparse_pa_decode_ws_need(kv->dtype, num_rows, k_pages);
+  if (need > kScratchBytes) return BSP_ERR_WORKSPACE;
+  if (need > 0 &&
       cudaMemsetAsync(scratch, 0, bsp::sparse_pa_counter_bytes(num_rows), reinterpret_cast<cudaStream_t>(stream)) !=
           cudaSuccess)
     return BSP_ERR_CUDA;

@@ -293,6 +293,11 @@ bsp_status bsp_topk_select(const float* scores, int32_t num_rows, int32_t max_pa
  * need separate workspaces.
  * ---------------------------------------------------------------------- */
 size_t bsp_sparse_pa_decode_workspace_bytes(int32_t num_rows, int32_t k_pages, int32_t group);
+/* The number of CTAs (splits) each row of a decode call with these sizes runs
+ * on, for KV format kv_dtype on the current device: 1 (one CTA finishes the
+ * row), 2..8 (the splits merge on chip in one thread-block cluster) or more
+ * (they merge through the workspace).  0 for invalid arguments. */
+int32_t bsp_sparse_pa_decode_splits(int32_t kv_dtype, int32_t num_rows, int32_t k_pages);
 bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
                                 const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
                                 int32_t k_pages, float sm_scale, void* out, void* ws, size_t ws_bytes,
@@ -308,17 +313,21 @@ bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q
  * callers.
  *  - The workspace is a scratch array inside the library, a file-scope
  *    __device__ array of 16 MiB that every GPU loading the library holds
- *    until the process exits.  A call whose split-K plan needs more
- *    (bsp_sparse_pa_decode_workspace_bytes(rows, k_pages, G) > 16 MiB) returns
- *    BSP_ERR_WORKSPACE and enqueues nothing.
+ *    until the process exits.  A call whose split-K plan for this KV format
+ *    needs more returns BSP_ERR_WORKSPACE and enqueues nothing (the plan
+ *    uses a workspace only for fewer rows than SMs / 8 with more than 8
+ *    splits a row, at most 64 splits of 8320 B: about 10 MB on 152 SMs).
  *  - The first call on a device looks up the array's address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
- *  - Calls share the array and it keeps the last call's contents; each call
- *    first clears the part that must start at zero (the split-K arrival
- *    counters, an async memset on `stream`).  Calls that overlap on the GPU
- *    (other streams, other host threads) race on it and must be serialised
- *    by the caller.
+ *    before any stream capture.  The address is cached per device and does
+ *    not survive cudaDeviceReset: after a reset, do not call this again in
+ *    the same process.
+ *  - Calls share the array and it keeps the last call's contents.  When the
+ *    plan uses the workspace, a call first clears the part that must start at
+ *    zero (the split-K arrival counters, an async memset on `stream`); a
+ *    plan that merges on chip touches the array not at all.  Calls that
+ *    overlap on the GPU (other streams, other host threads) race on it and
+ *    must be serialised by the caller.
  *  - It calls no allocator (no cudaMalloc / cudaFree).  Arguments and errors
  *    are those of bsp_sparse_pa_decode.
  * ---------------------------------------------------------------------- */

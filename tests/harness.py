@@ -123,21 +123,35 @@ def bf16_f32(t):
     return O.bf16_to_f32(t.cpu().numpy().view(np.uint16))
 
 
-def bf16_ulp(x):
-    """Spacing of bf16 numbers at |x| (8 significant bits)."""
-    a = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
-    return 2.0 ** (np.floor(np.log2(a)) - 7)
+def _bf16_bits(x):
+    return (np.ascontiguousarray(x, np.float32).view(np.uint32) >> 16).astype(np.int64)
 
 
-def attention_close(got, ref, max_abs=1e-2, rel_l2=5e-3):
+def attention_close(got, ref, max_abs=1e-2, rel_l2=5e-3, label=""):
     """The attention tolerance on bf16 outputs after identical dequantisation:
-    relative L2 5e-3, and max-abs 1e-2 -- or one bf16 spacing of the
-    reference where that spacing is wider (|ref| >= 2.56), since the output is
-    itself rounded to bf16.  Returns (ok, worst |err| / allowed, rel-L2)."""
-    d = np.abs(got - ref)
-    allowed = np.maximum(max_abs, bf16_ulp(ref))
+    max-abs 1e-2 and relative L2 5e-3, as stated for the path.
+
+    Both sides round their result to bf16 at the end.  At |x| >= 2 one bf16
+    spacing (2^-6) is wider than 1e-2, so two correct results that straddle
+    a rounding boundary there differ by more than 1e-2.  Such elements are
+    not absorbed into a wider bound: an element over 1e-2 passes only if got
+    and ref are adjacent bf16 numbers of the same sign (one spacing apart,
+    which exceeds 1e-2 only at |x| >= 2), and every such exception is printed
+    by its flat index.  Returns (ok, worst |err| / 1e-2 over the other
+    elements, rel-L2)."""
+    got = np.asarray(got, np.float32)
+    ref = np.asarray(ref, np.float32)
+    d = np.abs(got.astype(np.float64) - ref.astype(np.float64))
     rl2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
-    worst = float((d / allowed).max()) if d.size else 0.0
+    adjacent = (np.abs(_bf16_bits(got) - _bf16_bits(ref)) == 1) & (np.signbit(got) == np.signbit(ref))
+    exc = (d > max_abs) & adjacent
+    if exc.any():
+        idx = np.flatnonzero(exc)
+        print(f"attention {label}: {idx.size} one-spacing exception(s) at |x| >= 2, flat index "
+              f"{idx[:20].tolist()}{' ...' if idx.size > 20 else ''}: got {got.ravel()[idx[:5]].tolist()} "
+              f"ref {ref.ravel()[idx[:5]].tolist()}")
+    rest = d[~exc]
+    worst = float(rest.max() / max_abs) if rest.size else 0.0
     return worst <= 1.0 and rl2 <= rel_l2, worst, rl2
 
 

@@ -63,3 +63,11 @@ def test_host_validation_without_a_gpu():
     assert L.bsp_index_score_prefill(C.byref(ic2), fake, bsp.BF16, fake, 4, fake, fake, 4, fake, 1, 1, 8, fake,
                                      None, None) == 2
     assert L.bsp_topk_select(fake, 4, 8, fake, fake, fake, 1, 0, 0, 1, fake, fake, fake, None) == 1  # k_pages 0
+    # the allocation-free attention runs the attention's own checks first: a
+    # group of 3 query heads per KV head is refused before any CUDA call
+    d2 = bsp.KvCacheDesc()
+    assert L.bsp_kv_cache_interleaved(bsp.FP8_E4M3, 2, fake, 16, 0.5, 0.5, C.byref(d2)) == 0
+    assert L.bsp_sparse_pa_decode_noalloc(C.byref(d2), fake, bsp.BF16, 6, fake, fake, 4, 8, C.c_float(0.1), fake,
+                                          None, None) == 2
+    assert L.bsp_sparse_pa_decode_noalloc(C.byref(d2), fake, bsp.BF16, 32, fake, fake, 3, 8, C.c_float(0.1), fake,
+                                          None, None) == 1  # rows not a multiple of the KV heads

@@ -1,13 +1,15 @@
 """Parity at the benchmark's full sizes (GPU required): each workload's step
 runs exactly as bench.py runs it -- the CUDA writer fills every sequence's
-caches, then one DecodeStep (workloads 2-4) or MixedStep (workloads 5-6) -- and
-a sample of rows is checked against the oracle, which writes and scores only
-the sampled sequences:
+caches, then one DecodeStep (workloads 2-4) or MixedStep (workloads 5-6).
+Every row's length, and every row's selection (top-k pages, page ids and
+context length) is checked bit for bit against the oracle's top-k run on the
+GPU's own score rows.  A sample of rows is then checked against the oracle,
+which writes and scores only the sampled sequences:
   cache bytes of the sampled sequences' blocks equal, byte for byte;
   page scores within 2e-5 * sum_d |q_d k_d|, the same -inf pattern;
   selections equal up to near-ties (gap-aware);
-  attention outputs within max-abs 1e-2 (or one bf16 spacing) and
-  relative-L2 5e-3 of the oracle fed the GPU's sparse table.
+  attention outputs within max-abs 1e-2 and relative-L2 5e-3 of the oracle
+  fed the GPU's sparse table.
 """
 import numpy as np
 import pytest
@@ -57,12 +59,26 @@ def test_full_size_step_on_sampled_rows(config):
     torch.cuda.synchronize()
     assert st.dev_err.item() == 0
 
-    # the oracle side on the sampled rows' sequences
-    rows = _sample_rows(w, np.random.default_rng(config))
+    # every row: the row lengths, and the selection the oracle's top-k makes
+    # from the GPU's own score rows, bit for bit (table ids and lengths too)
     rs_all, rl_all = O.row_lengths_decode(w.decode_lens, w.q_len, w.hkv)
     if w.num_rows > w.num_decode_rows:
         rs_p, rl_p = O.row_lengths_prefill(w.query_req_id, w.query_abs_pos, w.hkv)
         rs_all, rl_all = np.concatenate([rs_all, rs_p]), np.concatenate([rl_all, rl_p])
+    assert np.array_equal(st.row_seq.cpu().numpy(), rs_all)
+    assert np.array_equal(st.row_len.cpu().numpy(), rl_all)
+    got = st.scores.cpu().numpy()
+    ti_all, sb_all, ctx_all = O.topk_select(got, rs_all, rl_all, w.block_table, 1 if w.kv_dtype == W.MXFP4 else 0,
+                                            w.k_pages, True)
+    for name, ref_t, gpu_t in (("topk_idx", ti_all, st.topk_idx), ("sparse_bt", sb_all, st.sparse_bt),
+                               ("sparse_ctx", ctx_all, st.sparse_ctx)):
+        g_np = gpu_t.cpu().numpy()
+        bad = np.flatnonzero((g_np != ref_t).reshape(len(g_np), -1).any(axis=1))
+        assert bad.size == 0, f"{name}: {bad.size} of {len(g_np)} rows differ, first {bad[:8].tolist()}"
+    print(f"workload {config}: selections of all {w.num_rows} rows bit-exact against the oracle's top-k")
+
+    # the oracle side on the sampled rows' sequences
+    rows = _sample_rows(w, np.random.default_rng(config))
     seqs = sorted(set(int(rs_all[r]) for r in rows))
     okv = np.zeros(w.num_blocks * O.kv_block_bytes(w.kv_dtype, w.hkv), np.uint8)
     oidx = np.zeros(w.num_blocks * w.hidx * O.index_field_bytes(w.idx_dtype), np.uint8)
@@ -88,7 +104,6 @@ def test_full_size_step_on_sampled_rows(config):
     iq_o = iq if w.idx_q_dtype == W.BF16 else O.cast_e4m3(iq)
     ref, mag = O.index_score(w.idx_dtype, w.hidx, oidx, iq_o, w.idx_q_dtype, w.block_table, rs_all, rl_all,
                              w.max_pages, rows=rows, want_absdot=True)
-    got = st.scores.cpu().numpy()
     ti, _, _ = O.topk_select(ref, rs_all, rl_all, w.block_table, 1 if w.kv_dtype == W.MXFP4 else 0, w.k_pages, True,
                              rows=rows)
     gti = st.topk_idx.cpu().numpy()
@@ -106,6 +121,6 @@ def test_full_size_step_on_sampled_rows(config):
                                  ctx_gpu, SM_SCALE, rows=rows)
     ref_o = O.bf16_to_f32(out_ref).reshape(-1, w.group, 128)[rows]
     got_o = bf16_f32(st.out).reshape(-1, w.group, 128)[rows]
-    ok, worst, rl2 = attention_close(got_o, ref_o)
-    print(f"workload {config}: {len(rows)} rows, attention worst err/allowed {worst:.3g}, rel-L2 {rl2:.3g}")
+    ok, worst, rl2 = attention_close(got_o, ref_o, label=f"workload {config}")
+    print(f"workload {config}: {len(rows)} rows, attention worst err/1e-2 {worst:.3g}, rel-L2 {rl2:.3g}")
     assert ok, (worst, rl2)
