@@ -13,9 +13,12 @@ per KV head, top-128 pages (2048 tokens).  --config selects the others (1: the
 tiny bf16 case, 2: 32 fp8 sequences of 4096..8192 tokens, 4: MXFP4 64 x 128k,
 5/6: the chunked-prefill batch with an fp8 / MXFP4 index).
 
-Timing: every step is bracketed by CUDA events on the launching stream; an L2
-flush (a 256 MiB memset, twice the L2) runs before each step and is not
-timed; the reported ms_per_step is the mean of the K event intervals, max over
+Timing: every step is bracketed by CUDA events on the launching stream.
+Between steps L2 is flushed (a 256 MiB memset, twice the L2, not timed),
+unless the step's algorithmic bytes are at least 4x the L2: then the inputs
+are larger than L2 and nothing is flushed (a write flush would leave L2 full of
+dirty lines the step then pays to write back); `config.l2` says which.  The
+reported ms_per_step is the mean of the K event intervals, max over
 ranks.  Consecutive kernels of a step overlap their launch (programmatic
 dependent launch), so no event sits between them in those K steps.  The K
 steps then run once more with an event between kernels, which gives each
@@ -59,6 +62,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "clean", "none"],
+                    help="between steps: flush L2 by a 256 MiB write (flush), by a write then a read that leaves "
+                         "it clean (clean), or not at all (none); auto: none when the step's algorithmic bytes are "
+                         "at least 4x the L2 (the inputs are larger than L2), else flush")
     ap.add_argument("--select-blocks", action="store_true",
                     help="128-token blocks as the unit of selection (top_k_pages / 8 blocks a row)")
     return ap.parse_args()
@@ -172,7 +179,39 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def workload_desc(w, select_blocks=False):
+L2_BYTES = 126.5 * 2**20  # GB300
+
+
+def decode_context_total(w):
+    """Tokens the decode rows attend (the sum of sparse_ctx), from the row
+    lengths alone: k' = min(k, n) pages, the tail page always among them."""
+    total = 0
+    for L in w.decode_lens:
+        for j in range(w.q_len):
+            r = max(0, int(L) - (w.q_len - 1 - j))
+            n = (r + 15) // 16
+            if n:
+                total += (16 * (min(w.k_pages, n) - 1) + r - 16 * (n - 1)) * w.hkv
+    return total
+
+
+def l2_policy(w, mode):
+    """auto: no flush when the step's algorithmic bytes are at least 4x the
+    L2 (its inputs are larger than L2), else a write flush."""
+    if mode != "auto":
+        return mode
+    step_bytes = index_algorithmic_bytes(w) + attention_algorithmic_bytes(w, decode_context_total(w))
+    return "none" if step_bytes >= 4 * L2_BYTES else "flush"
+
+
+L2_DESC = {
+    "flush": "flushed before every step (256 MiB memset, excluded from the step time)",
+    "clean": "flushed before every step (256 MiB memset then a 256 MiB read, excluded from the step time)",
+    "none": "not flushed: the inputs are larger than L2 (the step's algorithmic bytes are at least 4x the L2)",
+}
+
+
+def workload_desc(w, select_blocks=False, l2_mode="flush"):
     lens = w.decode_lens
     d = {"workload": w.name, "decode_seqs": int(w.num_decode), "q_len": int(w.q_len),
          "context_min": int(lens.min()) if len(lens) else 0, "context_max": int(lens.max()) if len(lens) else 0,
@@ -182,7 +221,7 @@ def workload_desc(w, select_blocks=False):
     if w.prefill_chunks:
         d["prefill_chunks"] = [list(c) for c in w.prefill_chunks]
         d["pad_rows"] = int(w.num_pad_tokens)
-    d["l2"] = "flushed before every step (256 MiB memset, excluded from the step time)"
+    d["l2"] = L2_DESC.get(l2_mode, l2_mode)
     d["selection_unit"] = "128-token block" if select_blocks else "16-token page"
     return d
 
@@ -288,7 +327,7 @@ def run_reference(args):
     line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": workload_desc(w, args.select_blocks),
+            "config": workload_desc(w, args.select_blocks, l2_policy(w, args.l2)),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
                              "sample": o.desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -333,6 +372,14 @@ def run_ours(args):
               "seq_lens": t(w.decode_lens)}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    l2_mode = l2_policy(w, args.l2)
+
+    def flush_l2():
+        if l2_mode in ("flush", "clean"):
+            flush.zero_()
+        if l2_mode == "clean":
+            flush.sum(dtype=torch.int64)
+
     K, Wm = args.steps, args.warmup
     nev = 5
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
@@ -342,7 +389,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     def one(evs=None, inner=False):
-        flush.zero_()
+        flush_l2()
         if evs is not None and not inner:
             evs[0].record(stream)
         st.run(inputs["k"], inputs["v"], inputs["idx_k"], inputs["slot"], inputs["q"], inputs["idx_q"],
@@ -441,11 +488,11 @@ def run_ours(args):
         def time_host(hs):
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
             for _ in range(3):
-                flush.zero_()
+                flush_l2()
                 hs.run(stream)
             torch.cuda.synchronize()
             for i in range(Ke):
-                flush.zero_()
+                flush_l2()
                 ev[i][0].record(stream)
                 hs.run(stream)
                 ev[i][1].record(stream)
@@ -472,7 +519,7 @@ def run_ours(args):
         line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "e4m3" if w.kv_dtype == 1 else ("mxfp4" if w.kv_dtype == 2 else "bf16"),
-                "data": "synthetic", "config": workload_desc(w, args.select_blocks), "roofline": roof, "kernels": kernels,
+                "data": "synthetic", "config": workload_desc(w, args.select_blocks, l2_mode), "roofline": roof, "kernels": kernels,
                 "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": launches,
                 "device_errors": err}
         print(json.dumps(line))

@@ -173,6 +173,37 @@ __device__ __forceinline__ uint32_t float2_to_e2m1x2(float first, float second) 
 __device__ __forceinline__ float e8m0_to_float(uint32_t b) {
   return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
 }
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// near 2^-22, results below 2^-126 flushed to zero, 2^-inf = 0).  For
+// softmax weights, which are rounded to f16 or bf16 before they are used.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// max of three floats in one instruction (PTX max.f32 with three sources)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (a.x * b.x, a.y * b.y), each rounded to nearest as a scalar multiply, in
+// one packed instruction
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t x, y, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+// largest of 16 values, as a tree of three-input maxima
+__device__ __forceinline__ float max16(const float (&x)[16]) {
+  const float a = fmax3(x[0], x[1], x[2]), b = fmax3(x[3], x[4], x[5]), c = fmax3(x[6], x[7], x[8]);
+  const float d = fmax3(x[9], x[10], x[11]), e = fmax3(x[12], x[13], x[14]);
+  return fmax3(fmax3(a, b, c), fmax3(d, e, x[15]), -INFINITY);
+}
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

@@ -17,13 +17,16 @@
 //   - tcgen05.mma.cta_group::1.kind::f8f6f4, M = 128 queries, N = 256 keys,
 //     K = 4 x 32 dims, into one of two 256-column fp32 TMEM accumulators;
 //     tcgen05.commit releases the key stage and signals the accumulator.
-// Warps 1..8 are the epilogue: warp w reads TMEM lanes 32*(w%4).. (its
-// quarter) and half of the 256 columns with tcgen05.ld, multiplies by the
-// per-token fp32 scales (which the producer copies per tile into one of two
-// shared-memory slots with a 1-D TMA, next to the accumulator), masks keys at
-// or past the row's causal length, max-pools 16 keys into a page score and
-// stores 8 pages per row per tile.  Accumulator double-buffering lets the
-// MMAs of the next tile run under the epilogue of this one.
+// Warps 1..16 are the epilogue: warp w reads TMEM lanes 32*(w%4).. (its
+// quarter) and a quarter of the 256 columns (64 keys = 4 pages) with two
+// tcgen05.ld in flight, multiplies by the per-token fp32 scales (packed
+// f32x2 multiplies), masks keys at or past the row's causal length only on
+// the tile that crosses it, max-pools 16 keys into a page score by a tree of
+// three-input maxima and stores 4 pages per row per tile.  The producer
+// copies each tile's scales with its keys, by a 1-D TMA into a ring of 8
+// shared-memory slots, so they land as early as the keys and never hold the
+// accumulators up.  Accumulator double-buffering lets the MMAs of the next
+// tile run under the epilogue of this one.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -36,17 +39,21 @@ namespace {
 constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE4m3, kFmtE4m3, 256, 128);
 constexpr int kStages = 4;
 constexpr int kKeyBlocksPerCta = 64;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 32 * (1 + kEpiWarps);
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 B
+// key scales: a ring of slots, one per tile (256 keys), filled with the
+// tile's keys; a slot is reused 8 tiles later, when its epilogue is long done
+constexpr int kScaleSlots = 8;
+constexpr int kNumBars = 1 + 2 * kStages + 4 + kScaleSlots;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kTileBytes /*A*/ + kStages * 2 * kTileBytes /*B*/ +
-                           2 * 256 * 4 /*scales*/ + 16 * 8 /*barriers*/ + 16;
+                           kScaleSlots * 256 * 4 /*scales*/ + kNumBars * 8 /*barriers*/ + 16;
 
 struct SmemLayout {
   uint8_t* a;
   uint8_t* b;  // [stage][256 rows][128 B]
-  float* scales;  // [2][256]
-  uint64_t* bars;  // a_full, b_full[S], b_empty[S], acc_full[2], acc_empty[2]
+  float* scales;  // [kScaleSlots][256]
+  uint64_t* bars;  // a_full, b_full[S], b_empty[S], acc_full[2], acc_empty[2], scale_full[kScaleSlots]
   uint32_t* tmem_slot;
 };
 
@@ -56,8 +63,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
   L.a = base;
   L.b = base + kTileBytes;
   L.scales = reinterpret_cast<float*>(L.b + kStages * 2 * kTileBytes);
-  L.bars = reinterpret_cast<uint64_t*>(L.scales + 2 * 256);
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 16);
+  L.bars = reinterpret_cast<uint64_t*>(L.scales + kScaleSlots * 256);
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + kNumBars);
   return L;
 }
 
@@ -71,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_empty = sm.bars + 1 + kStages;
   uint64_t* acc_full = sm.bars + 1 + 2 * kStages;
   uint64_t* acc_empty = sm.bars + 3 + 2 * kStages;
-  uint64_t* scale_full = sm.bars + 5 + 2 * kStages;  // [2]: a tile's key scales landed in sm.scales
+  uint64_t* scale_full = sm.bars + 5 + 2 * kStages;  // [kScaleSlots]: a tile's key scales landed
   __shared__ int s_tok0, s_tok1, s_lmax, s_seq;
   __shared__ int s_bid[kKeyBlocksPerCta];  // the key range's block ids (-1: missing)
 
@@ -106,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * kEpiWarps);
-      mbar_init(&scale_full[i], 1);
     }
+    for (int i = 0; i < kScaleSlots; ++i) mbar_init(&scale_full[i], 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -164,11 +171,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // key tile j (two blocks) into stage j % S, and its fp32 per-key
+      // scales (512 B a block) into scale slot j % kScaleSlots; that slot's
+      // previous tile, j - kScaleSlots, has finished its epilogue (the
+      // producer has already seen the epilogue of tile j - S - 1 release its
+      // accumulator)
       auto load_b = [&](int j) {
-        const int st = j % kStages;
+        const int st = j % kStages, ss = j % kScaleSlots;
         mbar_arrive_expect_tx(&b_full[st], 2 * kTileBytes);
         for (int h = 0; h < 2; ++h)
           tma_load_2d(sm.b + (st * 2 + h) * kTileBytes, &tmap_k, 0, block_row(kb0 + 2 * j + h), &b_full[st]);
+        fence_proxy_async();  // the slot's earlier readers (generic proxy) before the copy's writes
+        uint32_t bytes = 0;
+        for (int h = 0; h < 2; ++h) {
+          const int blk = kb0 + 2 * j + h;
+          if (blk < kb0 + nb && s_bid[blk - kb0] >= 0) bytes += 512;
+        }
+        mbar_arrive_expect_tx(&scale_full[ss], bytes);
+        for (int h = 0; h < 2; ++h) {
+          const int blk = kb0 + 2 * j + h;
+          if (blk < kb0 + nb && s_bid[blk - kb0] >= 0)
+            bulk_g2s(sm.scales + ss * 256 + 128 * h,
+                     p.idx_base + static_cast<int64_t>(s_bid[blk - kb0]) * p.block_stride + kFp8IndexScaleOff, 512,
+                     &scale_full[ss]);
+        }
       };
       mbar_arrive_expect_tx(a_full, kTileBytes);
       tma_load_2d(sm.a, &tmap_q, 0, tok0, a_full);
@@ -179,24 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % kStages, buf = j & 1;
         mbar_wait(&b_full[st], (j / kStages) & 1, p.err);
         mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
-        // the tile's fp32 key scales (512 B per block) into this buffer's
-        // scale slots: the epilogue of tile j-2 has released them
-        {
-          fence_proxy_async();
-          uint32_t bytes = 0;
-          for (int h = 0; h < 2; ++h) {
-            const int blk = kb0 + 2 * j + h;
-            if (blk < kb0 + nb && s_bid[blk - kb0] >= 0) bytes += 512;
-          }
-          mbar_arrive_expect_tx(&scale_full[buf], bytes);
-          for (int h = 0; h < 2; ++h) {
-            const int blk = kb0 + 2 * j + h;
-            if (blk < kb0 + nb && s_bid[blk - kb0] >= 0)
-              bulk_g2s(sm.scales + buf * 256 + 128 * h,
-                       p.idx_base + static_cast<int64_t>(s_bid[blk - kb0]) * p.block_stride + kFp8IndexScaleOff, 512,
-                       &scale_full[buf]);
-          }
-        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(sm.b + st * 2 * kTileBytes);
 #pragma unroll
@@ -204,62 +212,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_f8(tmem + buf * 256, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), kIdesc, k > 0);
         umma_commit(&b_empty[st]);
         umma_commit(&acc_full[buf]);
-        if (j + kStages < ntiles) {
-          mbar_wait(&b_empty[st], (j / kStages) & 1, p.err);
-          load_b(j + kStages);
+        // refill the previous tile's stage (its MMAs were issued an iteration
+        // ago), so the MMAs just issued queue behind them without a wait
+        const int jp = j - 1;
+        if (jp >= 0 && jp + kStages < ntiles) {
+          mbar_wait(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
+          load_b(jp + kStages);
         }
       }
     }
     __syncwarp();
   } else {
-    const int col0 = 128 * ((warp - 1) >> 2);  // this warp's half of the 256 columns
+    const int col0 = 64 * ((warp - 1) >> 2);  // this warp's quarter of the 256 columns (4 pages)
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
       // the tile's key scales (a missing block leaves stale but finite
       // scales: its keys lie past every row's length and are masked)
-      mbar_wait(&scale_full[buf], (j >> 1) & 1, p.err);
+      mbar_wait(&scale_full[j % kScaleSlots], (j / kScaleSlots) & 1, p.err);
       mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      float pv[8];
-      const int key0 = (kb0 + 2 * j) * kBlock;
+      float v[64];
+      tmem_ld32x2(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * 256 + col0, v);
+      const float* sc = sm.scales + (j % kScaleSlots) * 256 + col0;
+      const int kcol0 = (kb0 + 2 * j) * kBlock + col0;  // key of this warp's first column
+      const bool whole = kcol0 + 64 <= L;  // every key of the 4 pages inside the row's causal length
+      float pv[4];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float v[32];
-        const int c0 = col0 + 32 * cc;
-        tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * 256 + c0, v);
-        const float* sc = sm.scales + buf * 256 + c0;
-        if (key0 + c0 + 32 <= L) {  // every key of the chunk is inside the row's causal length
+      for (int pg = 0; pg < 4; ++pg) {
+        float x[16];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) m = fmaxf(m, v[16 * hh + c] * sc[16 * hh + c]);
-            pv[2 * cc + hh] = m;
-          }
-        } else {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            float m = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = c0 + 16 * hh + c;
-              const float x = v[16 * hh + c] * sc[16 * hh + c];
-              m = key0 + col < L ? fmaxf(m, x) : m;
-            }
-            pv[2 * cc + hh] = m;
-          }
+        for (int c = 0; c < 8; ++c) {
+          const float2 pr = fmul2(make_float2(v[16 * pg + 2 * c], v[16 * pg + 2 * c + 1]),
+                                  *reinterpret_cast<const float2*>(sc + 16 * pg + 2 * c));
+          x[2 * c] = pr.x, x[2 * c + 1] = pr.y;
         }
+        if (!whole) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) x[c] = kcol0 + 16 * pg + c < L ? x[c] : -INFINITY;
+        }
+        pv[pg] = max16(x);
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      mbar_arrive(&acc_empty[buf]);
+      mbar_arrive(&acc_empty[buf]);  // the accumulator is free again
       if (row_ok) {
         const int pg0 = (kb0 + 2 * j) * kPagesPerSide + col0 / kPage;
         float* dst = p.scores + static_cast<int64_t>(tok) * p.max_pages + pg0;
-        if (pg0 + 8 <= p.max_pages && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-          reinterpret_cast<float4*>(dst)[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-          reinterpret_cast<float4*>(dst)[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+        if (pg0 + 4 <= p.max_pages && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+          *reinterpret_cast<float4*>(dst) = make_float4(pv[0], pv[1], pv[2], pv[3]);
         } else {
-          for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 4; ++i)
             if (pg0 + i < p.max_pages) dst[i] = pv[i];
         }
       }

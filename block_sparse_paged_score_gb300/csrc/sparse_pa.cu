@@ -15,7 +15,8 @@
 // head; MXFP4: the 1 KB data and 64 B scales of both sides) completing on
 // mbarriers, and keeps its own online softmax.  Per 16-token page:
 //   S  = Q Kt : 2 n-tiles (8 tokens) x 8 k-steps of mma.sync m16n8k16
-//   P  = exp2(S*scale - m)   (log2 domain, running max m and sum l per head)
+//   P  = 2^(S*scale - m)     (log2 domain, running max m and sum l per head;
+//                             the hardware ex2.approx)
 //   O += P V  : 16 n-tiles (8 dims) of mma.sync m16n8k16
 // The Q fragments sit in shared memory (loaded once per CTA), which keeps the
 // fp8 kernel within 128 registers: four CTAs (16 warps) per SM.  fp8 pages
@@ -330,15 +331,15 @@ __device__ __forceinline__ void pa_page(PaState& a, uint32_t qs, uint32_t kaddr,
   // some row's max moved.  softmax = exp2(s - m) / sum is the same for any m.
   const bool move0 = mx0 > a.m0 + kRescaleLog2, move1 = mx1 > a.m1 + kRescaleLog2;
   const float mn0 = move0 ? mx0 : a.m0, mn1 = move1 ? mx1 : a.m1;
-  const float al0 = exp2f(a.m0 - mn0), al1 = exp2f(a.m1 - mn1);
+  const float al0 = ex2_approx(a.m0 - mn0), al1 = ex2_approx(a.m1 - mn1);
   a.m0 = mn0, a.m1 = mn1;
   float pr[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    pr[nt][0] = exp2f(s[nt][0] - mn0);
-    pr[nt][1] = exp2f(s[nt][1] - mn0);
-    pr[nt][2] = exp2f(s[nt][2] - mn1);
-    pr[nt][3] = exp2f(s[nt][3] - mn1);
+    pr[nt][0] = ex2_approx(s[nt][0] - mn0);
+    pr[nt][1] = ex2_approx(s[nt][1] - mn0);
+    pr[nt][2] = ex2_approx(s[nt][2] - mn1);
+    pr[nt][3] = ex2_approx(s[nt][3] - mn1);
   }
   a.l0 = a.l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);
   a.l1 = a.l1 * al1 + (pr[0][2] + pr[0][3] + pr[1][2] + pr[1][3]);
