@@ -9,22 +9,28 @@
 //   scores[i, p] = max_{t in page p, t < L_i} S[i, t],  -inf past ceil(L_i/16)
 //
 // One CTA = one tile of 128 consecutive query rows of one chunk x a range of
-// 64 key blocks, as the fp8 prefill scorer.  Warp 0, lane 0 is the producer
-// and MMA issuer:
-//   - the query tile (e4m3) by a 2-D TMA load with 128-byte swizzle;
-//   - each half block of 64 keys by a 2-D TMA load of 4-bit data type
+// 64 key blocks, as the fp8 prefill scorer; a key tile is one 128-token
+// block.  The group scales go to the tensor core itself: each key tile is
+// four tcgen05.mma kind::mxf8f6f4.block_scale (A = queries, e4m3, M = 128;
+// B = keys, e2m1, N = 128; K = 32 = one scale group each, the descriptor's
+// scale-factor id picking group g's byte) accumulating into one fp32 TMEM
+// accumulator of 128 columns, double-buffered.
+//   - warp 0, lane 0: the query tile by a 2-D TMA load with 128-byte
+//     swizzle; each key block by a 2-D TMA load of 4-bit data type
 //     16U4_ALIGN16B (every 8 packed bytes of 16 e2m1 values unpacked into a
-//     16-byte slot, the layout kind::f8f6f4 reads), 128-byte swizzle; its
-//     64 x 4 e8m0 scales by a 1-D copy into one of two scale slots beside the
-//     accumulator they belong to;
-//   - four tcgen05.mma kind::f8f6f4 (A = queries, M = 128; B = keys, N = 64;
-//     K = 32 = one scale group each) into four fp32 accumulators of 64 TMEM
-//     columns, double-buffered (2 x 256 columns).
-// Warps 1..8 are the epilogue: warp w reads TMEM lanes 32*(w%4).. (its
-// quarter of the query rows) and half of the 64 keys, scales the four group
-// sums of each key by its 2^(e-127) (decoded once per tile into shared
-// memory by the epilogue warps together), masks keys at or past the row's
-// causal length and max-pools 16 keys into a page score.
+//     16-byte slot, the layout the f8f6f4 kinds read), 128-byte swizzle,
+//     into a 4-stage ring; the MMAs;
+//   - warps 1..4: the scale factors in TMEM.  A cell of 32 bits holds the
+//     four group scales of one key (the field stores them so: 4 bytes a
+//     key); key n's cell goes to lane 32p + n % 32 of every 32-lane
+//     sub-partition p, column (slot) + n / 32.  Each of the four warps
+//     writes its own sub-partition's copy with tcgen05.st, one scale slot of
+//     4 columns per ring stage, and the query scales (all 1.0) once;
+//   - warps 5..12: the epilogue.  Warp w reads TMEM lanes 32*(w%4).. (its
+//     quarter of the query rows) and 64 of the 128 keys (4 pages) with two
+//     tcgen05.ld in flight, masks keys at or past the row's causal length on
+//     the tile that crosses it and max-pools 16 keys into a page score (a
+//     tree of three-input maxima); there is no per-key multiply left.
 //
 // Every wait is bounded; after a timed-out wait a role stops waiting (the
 // error word is set) and the CTA frees its TMEM and returns.
@@ -38,26 +44,24 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kKeyBlocksPerCta = 64;
-constexpr int kKeysPerTile = 64;
+constexpr int kKeys = 128;            // keys a tile (one block)
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (1 + kEpiWarps);
-constexpr int kAccCols = 4 * kKeysPerTile;  // four scale groups
-constexpr int kQTile = 128 * 128;           // 128 query rows x 128 B
-constexpr int kKeyTile = kKeysPerTile * 128;  // 64 keys x 128 padded bytes
-constexpr uint32_t kKeyTx = kKeysPerTile * 64;  // the packed bytes the tensor load reads
-constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE4m3, kFmtE2m1, kKeysPerTile, 128);
-constexpr int kSmemUsed = 1024 /*align slack*/ + kQTile + kStages * kKeyTile + 2 * 256 /*e8m0*/ +
-                          2 * 256 * 4 /*decoded scales*/ + 16 * 8 /*barriers*/ + 16;
+constexpr int kScaleWarps = 4;
+constexpr int kThreads = 32 * (1 + kScaleWarps + kEpiWarps);
+constexpr int kQTile = 128 * 128;     // 128 query rows x 128 B
+constexpr int kKeyTile = kKeys * 128;  // 128 keys x 128 padded bytes
+constexpr uint32_t kKeyTx = kKeys * 64;  // the packed bytes the tensor load reads
+// TMEM columns: two accumulators, the query scales, one key-scale slot per stage
+constexpr uint32_t kColSfa = 256, kColSfb = 288, kSfbStride = 32;
+constexpr int kSmemUsed = 1024 /*align slack*/ + kQTile + kStages * kKeyTile + 32 * 8 /*barriers*/ + 16;
 // one CTA per SM: each holds all 512 TMEM columns, so a second resident CTA
 // would only wait in tcgen05.alloc
 constexpr int kSmemBytes = kSmemUsed > 120 * 1024 ? kSmemUsed : 120 * 1024;
 
 struct SmemLayout {
   uint8_t* a;       // queries
-  uint8_t* b;       // [stage][64 keys][128 B]
-  uint8_t* e8;      // [2][64 keys][4] raw scales
-  float* scales;    // [2][64 keys][4] decoded
-  uint64_t* bars;   // a_full, b_full[S], b_empty[S], acc_full[2], acc_empty[2], scale_full[2]
+  uint8_t* b;       // [stage][128 keys][128 B]
+  uint64_t* bars;   // a_full, b_full[S], b_empty[S], sf_full[S], acc_full[2], acc_empty[2]
   uint32_t* tmem_slot;
 };
 
@@ -66,15 +70,10 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   L.a = base;
   L.b = base + kQTile;
-  L.e8 = L.b + kStages * kKeyTile;
-  L.scales = reinterpret_cast<float*>(L.e8 + 2 * 256);
-  L.bars = reinterpret_cast<uint64_t*>(L.scales + 2 * 256);
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 16);
+  L.bars = reinterpret_cast<uint64_t*>(L.b + kStages * kKeyTile);
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.bars + 32);
   return L;
 }
-
-// the epilogue warps' own barrier (named barrier 1, 256 threads)
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     index_score_prefill_mx_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -84,9 +83,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* a_full = sm.bars;
   uint64_t* b_full = sm.bars + 1;
   uint64_t* b_empty = sm.bars + 1 + kStages;
-  uint64_t* acc_full = sm.bars + 1 + 2 * kStages;
-  uint64_t* acc_empty = sm.bars + 3 + 2 * kStages;
-  uint64_t* scale_full = sm.bars + 5 + 2 * kStages;
+  uint64_t* sf_full = sm.bars + 1 + 2 * kStages;
+  uint64_t* acc_full = sm.bars + 1 + 3 * kStages;
+  uint64_t* acc_empty = sm.bars + 3 + 3 * kStages;
   __shared__ int s_tok0, s_tok1, s_lmax, s_seq;
   __shared__ int s_bid[kKeyBlocksPerCta];  // the key range's block ids (-1: missing)
 
@@ -116,11 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
+      mbar_init(&sf_full[i], 32 * kScaleWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 32 * kEpiWarps);
-      mbar_init(&scale_full[i], 1);
     }
     mbar_fence_init();
   }
@@ -129,31 +128,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tok0 < 0) return;  // past the last tile (the grid is an upper bound)
 
   // the epilogue's row and its causal length; the tile's longest row
+  const bool epi = warp >= 1 + kScaleWarps;
   const int quarter = warp & 3;
   const int row = 32 * quarter + lane;
   const int tok = tok0 + row;
-  const bool row_ok = warp >= 1 && tok < tok1;
+  const bool row_ok = epi && tok < tok1;
+  const bool first_epi = epi && warp < 1 + kScaleWarps + 4;  // one warp per quarter
   const int max_len = p.max_pages * kPage;
   int L = 0;
   if (row_ok) {
     L = min(max(p.row_len[tok], 0), max_len);
     if (p.row_seq[tok] != s_seq) set_err(p.err, BSP_DEVERR_GROUP_SEQ);
-    if (warp <= 4) atomicMax(&s_lmax, L);
+    if (first_epi) atomicMax(&s_lmax, L);
   }
   __syncthreads();
-  const int nb = max(0, min(kKeyBlocksPerCta, (s_lmax + kBlock - 1) / kBlock - kb0));
-  const int ntiles = 2 * nb;  // half blocks of 64 keys
+  const int ntiles = max(0, min(kKeyBlocksPerCta, (s_lmax + kBlock - 1) / kBlock - kb0));
   const int page_end = min((kb0 + kKeyBlocksPerCta) * kPagesPerSide, p.max_pages);
   const int seq = s_seq;
 
   if (ntiles == 0) {
-    if (row_ok && warp <= 4)
+    if (row_ok && first_epi)
       for (int pg = kb0 * kPagesPerSide; pg < page_end; ++pg)
         p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
     return;
   }
 
-  if (tid < nb) {
+  if (tid < ntiles) {
     int bid = p.block_table[static_cast<int64_t>(seq) * p.bt_stride + kb0 + tid];
     if (bid < 0 || bid >= p.num_blocks) {
       set_err(p.err, BSP_DEVERR_BLOCK_ID);
@@ -169,16 +169,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *sm.tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+  if (warp >= 1 && warp <= kScaleWarps) {  // the queries' scales: all 1.0, in each sub-partition's copy
+    tmem_st4(tmem + lane_base + kColSfa, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
-      // key tile j: keys 64*(j%2).. of block kb0 + j/2
+      // key tile j = block kb0 + j
       auto load_b = [&](int j) {
         const int st = j % kStages;
-        const int bid = s_bid[j >> 1];
-        const int r0 = bid < 0 ? oob_row
-                               : static_cast<int>(static_cast<int64_t>(bid) * (p.block_stride / 64) +
-                                                  (j & 1) * kKeysPerTile);
+        const int bid = s_bid[j];
+        const int r0 = bid < 0 ? oob_row : static_cast<int>(static_cast<int64_t>(bid) * (p.block_stride / 64));
         mbar_arrive_expect_tx(&b_full[st], kKeyTx);
         tma_load_2d(sm.b + st * kKeyTile, &tmap_k, 0, r0, &b_full[st]);
       };
@@ -191,26 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < ntiles && alive; ++j) {
         const int st = j % kStages, buf = j & 1;
         alive = mbar_wait(&b_full[st], (j / kStages) & 1, p.err) &&
+                mbar_wait(&sf_full[st], (j / kStages) & 1, p.err) &&
                 mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
         if (!alive) break;
-        {  // the tile's e8m0 scales (64 keys x 4 B) into this buffer's slot
-          const int bid = s_bid[j >> 1];
-          fence_proxy_async();
-          mbar_arrive_expect_tx(&scale_full[buf], bid >= 0 ? 256 : 0);
-          if (bid >= 0)
-            bulk_g2s(sm.e8 + buf * 256,
-                     p.idx_base + static_cast<int64_t>(bid) * p.block_stride + kMxScaleOff + (j & 1) * 256, 256,
-                     &scale_full[buf]);
-        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(sm.b + st * kKeyTile);
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          umma_f8(tmem + buf * kAccCols + kKeysPerTile * g, smem_desc_sw128(a_addr + 32 * g),
-                  smem_desc_sw128(b_addr + 32 * g), kIdesc, 0);
+          umma_mx(tmem + buf * kKeys, smem_desc_sw128(a_addr + 32 * g), smem_desc_sw128(b_addr + 32 * g),
+                  idesc_mxf8f6f4(kFmtE4m3, kFmtE2m1, kKeys, 128, g, g), tmem + kColSfa,
+                  tmem + kColSfb + kSfbStride * st, g > 0);
         umma_commit(&b_empty[st]);
         umma_commit(&acc_full[buf]);
-        const int jp = j - 1;  // refill the previous tile's slot (its MMAs were issued an iteration ago)
+        const int jp = j - 1;  // refill the previous tile's stage (its MMAs were issued an iteration ago)
         if (jp >= 0 && jp + kStages < ntiles) {
           alive = mbar_wait(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
           if (alive) load_b(jp + kStages);
@@ -219,60 +217,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (alive) mbar_wait(&b_empty[(ntiles - 1) % kStages], ((ntiles - 1) / kStages) & 1, p.err);
     }
     __syncwarp();
+  } else if (warp <= kScaleWarps) {
+    // key tile j's scale cells into slot j % S: lane l holds keys l, 32 + l,
+    // 64 + l, 96 + l (columns 0..3 of the slot); every sub-partition its copy
+    bool alive = true;
+    for (int j = 0; j < ntiles && alive; ++j) {
+      const int st = j % kStages;
+      if (j >= kStages) alive = mbar_wait(&b_empty[st], ((j / kStages) - 1) & 1, p.err);  // the slot's MMAs are done
+      if (!alive) break;
+      const int bid = s_bid[j];
+      uint32_t w[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};  // a missing block: zero keys, unit scales
+      if (bid >= 0) {
+        const uint32_t* cells = reinterpret_cast<const uint32_t*>(
+            p.idx_base + static_cast<int64_t>(bid) * p.block_stride + kMxScaleOff);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = cells[32 * c + lane];
+      }
+      tmem_st4(tmem + lane_base + kColSfb + kSfbStride * st, w[0], w[1], w[2], w[3]);
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(&sf_full[st]);
+    }
   } else {
-    const int half = (warp - 1) >> 2;  // this warp's 32 of the tile's 64 keys
-    const int et = tid - 32;           // 0..255 among the epilogue threads
-    // every epilogue thread runs every iteration (the named barrier needs all
-    // 256); after a timed-out wait a warp stops waiting and reading TMEM
+    const int half = (warp - 1 - kScaleWarps) >> 2;  // this warp's 64 of the tile's 128 keys
     bool alive = true;
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
-      if (alive) alive = __all_sync(0xffffffffu, mbar_wait(&scale_full[buf], (j >> 1) & 1, p.err));
-      if (alive) {  // decode the tile's 256 scales once, shared by every row
-        const uint8_t e = sm.e8[buf * 256 + et];
-        sm.scales[buf * 256 + et] = e8m0_to_float(e);
-      }
-      epi_sync();  // the decoded scales, for every row; and buffer buf^1's readers are done
-      if (alive) alive = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err));
-      if (!alive) continue;
+      if (alive) alive = mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
+      if (!alive) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * kAccCols + 32 * half;
-      float a0[32], a1[32], a2[32], a3[32];
-      tmem_ld32(taddr, a0);
-      tmem_ld32(taddr + kKeysPerTile, a1);
-      tmem_ld32(taddr + 2 * kKeysPerTile, a2);
-      tmem_ld32(taddr + 3 * kKeysPerTile, a3);
+      float v[64];
+      tmem_ld32x2(tmem + lane_base + buf * kKeys + 64 * half, v);
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       mbar_arrive(&acc_empty[buf]);
-      const float4* sc = reinterpret_cast<const float4*>(sm.scales + buf * 256) + 32 * half;
-      const int key0 = (kb0 + (j >> 1)) * kBlock + (j & 1) * kKeysPerTile + 32 * half;
-      float pv[2];
+      const int key0 = (kb0 + j) * kBlock + 64 * half;
+      const bool whole = key0 + 64 <= L;  // every key of the 4 pages inside the row's causal length
+      float pv[4];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float m = -INFINITY;
+      for (int pg = 0; pg < 4; ++pg) {
+        float x[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int k = 16 * hh + c;
-          const float4 f = sc[k];
-          float v = a0[k] * f.x;
-          v = fmaf(a1[k], f.y, v);
-          v = fmaf(a2[k], f.z, v);
-          v = fmaf(a3[k], f.w, v);
-          m = key0 + k < L ? fmaxf(m, v) : m;
-        }
-        pv[hh] = m;
+        for (int c = 0; c < 16; ++c) x[c] = (whole || key0 + 16 * pg + c < L) ? v[16 * pg + c] : -INFINITY;
+        pv[pg] = max16(x);
       }
       if (row_ok) {
         const int pg0 = key0 / kPage;
         float* dst = p.scores + static_cast<int64_t>(tok) * p.max_pages + pg0;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-          if (pg0 + hh < p.max_pages) dst[hh] = pv[hh];
+        if (pg0 + 4 <= p.max_pages && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+          *reinterpret_cast<float4*>(dst) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+        } else {
+          for (int i = 0; i < 4; ++i)
+            if (pg0 + i < p.max_pages) dst[i] = pv[i];
+        }
       }
     }
     // pages of this key range that no tile covered
-    if (row_ok && warp <= 4)
-      for (int pg = (kb0 + nb) * kPagesPerSide; pg < page_end; ++pg)
+    if (row_ok && first_epi)
+      for (int pg = (kb0 + ntiles) * kPagesPerSide; pg < page_end; ++pg)
         p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
   }
 
@@ -290,7 +290,7 @@ cudaError_t launch_index_score_prefill_mx(const PrefillScoreParams& p, cudaStrea
   CUtensorMap tq, tk;
   const uint64_t key_rows = static_cast<uint64_t>(p.num_blocks) * (p.block_stride / 64);
   if ((reinterpret_cast<uintptr_t>(p.idx_base) & 31) || p.block_stride % 64) return cudaErrorNotSupported;
-  if (!make_map_u8(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map_u4(&tk, p.idx_base, key_rows, 64))
+  if (!make_map_u8(&tq, p.q, static_cast<uint64_t>(p.num_rows)) || !make_map_u4(&tk, p.idx_base, key_rows, kKeys))
     return cudaErrorInvalidValue;
   static std::atomic<uint64_t> configured{0};
   {
