@@ -1,0 +1,148 @@
+"""Microbenchmarks of the GB300 units behind the sparse path's kernel choices.
+
+    python bench_micro.py [gather] [mma] [umma] [cvt] [sf_layout]   (default: all)
+
+Prints one JSON line per measurement (CUDA events on the launching stream,
+best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
+  gather     GB/s of a 4 KB page-pair gather by 1-D TMA into shared memory,
+             from a pool that fits L2 (16..128 MB) or does not (1 GB): the
+             data-movement ceiling of an attention over selected pages
+  mma        TFLOP/s of mma.sync m16n8k16 f16 and m16n8k32 e4m3
+  umma       TFLOP/s of tcgen05.mma (one issuing thread, M = 128) by N, and
+             with N = 16 into several independent accumulators
+  cvt        e4m3x2 -> f16x2 conversions per clock per SM
+  sf_layout  checks where kind::mxf8f6f4.block_scale reads its scale
+             factors in TMEM: row r's cell at lanes 32p + r % 32 of every
+             sub-partition p, column base + r / 32 (the MXFP4 prefill scorer
+             relies on it)
+"""
+import ctypes as C
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+LIB = os.path.join(ROOT, "_build", "libbench_micro.so")
+
+
+def build():
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    src = os.path.join(ROOT, "bench_micro.cu")
+    if os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(src):
+        return LIB
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+                           "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-shared", "-I", ROOT, "-I",
+                           os.path.join(ROOT, "include"), src,
+                           "-o", LIB, "-lcuda"])
+    return LIB
+
+
+def main():
+    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "mma", "umma", "cvt", "sf_layout"]
+    L = C.CDLL(build())
+    vp, i32 = C.c_void_p, C.c_int
+    L.micro_gather.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+    L.micro_mma_sync.argtypes = [i32, i32, vp, i32, vp]
+    L.micro_umma.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+    L.micro_umma_multi.argtypes = [i32, i32, i32, vp, vp, vp]
+    L.micro_cvt.argtypes = [i32, i32, vp, vp]
+    L.micro_sf_layout.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+    dev = "cuda"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    s = torch.cuda.current_stream()
+    sp = C.c_void_p(s.cuda_stream)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(fn, reps=5):
+        assert fn() == 0
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return min(ts)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    if "gather" in which:
+        rng = np.random.default_rng(0)
+        for nblocks, rows in ((512, 16384), (4096, 16384), (32768, 16384), (32768, 512)):
+            pool = torch.zeros(nblocks * 32768, dtype=torch.uint8, device=dev)
+            # page ids of an interleaved fp8 cache: block*16 + j, j < 8 (K page; V 8 slots on)
+            ids = torch.from_numpy((rng.integers(0, nblocks, (rows, 128)) * 16 +
+                                    rng.integers(0, 8, (rows, 128))).astype(np.int32)).to(dev)
+            sink = torch.zeros(rows * 128, dtype=torch.int32, device=dev)
+            for ring in (2, 3, 4):
+                ms = timed(lambda: L.micro_gather(pool.data_ptr(), ids.data_ptr(), rows, 128, ring, sink.data_ptr(),
+                                                  err.data_ptr(), sp))
+                emit({"micro": "gather", "pool_MB": nblocks * 32768 / 2 ** 20, "rows": rows, "pages_per_row": 128,
+                      "ring": ring, "ms": ms, "GB_per_s": rows * 128 * 4096 / (ms / 1e3) / 1e9})
+            del pool
+    if "mma" in which:
+        out = torch.zeros(sms * 8 * 256, dtype=torch.float32, device=dev)
+        for e4m3 in (0, 1):
+            for cps in (2, 4, 8):
+                iters = 4000
+                ms = timed(lambda: L.micro_mma_sync(sms * cps, iters, out.data_ptr(), e4m3, sp))
+                flop = sms * cps * 8 * iters * 8 * (2 * 16 * 8 * (32 if e4m3 else 16))
+                emit({"micro": "mma_sync", "shape": "m16n8k32.e4m3" if e4m3 else "m16n8k16.f16",
+                      "warps_per_sm": cps * 8, "ms": ms, "TFLOP_per_s": flop / (ms / 1e3) / 1e12})
+    if "umma" in which:
+        sink = torch.zeros(sms * 128, dtype=torch.int32, device=dev)
+        for kind in (0, 1):
+            for n in (16, 32, 64, 128, 256):
+                iters = 20000 if n <= 64 else 5000
+                ms = timed(lambda: L.micro_umma(sms, iters, n, kind, err.data_ptr(), sink.data_ptr(), sp))
+                k = 16 if kind == 0 else 32
+                emit({"micro": "umma", "kind": "f16" if kind == 0 else "f8f6f4.e4m3", "M": 128, "N": n, "K": k,
+                      "ms": ms, "TFLOP_per_s": sms * iters * 2 * 128 * n * k / (ms / 1e3) / 1e12,
+                      "ns_per_mma": ms * 1e6 / iters})
+        for nacc in (1, 2, 4, 8, 16):
+            iters = 32000
+            ms = timed(lambda: L.micro_umma_multi(sms, iters, nacc, err.data_ptr(), sink.data_ptr(), sp))
+            emit({"micro": "umma_accumulators", "kind": "f16", "M": 128, "N": 16, "K": 16, "accumulators": nacc,
+                  "ms": ms, "TFLOP_per_s": sms * iters * 2 * 128 * 16 * 16 / (ms / 1e3) / 1e12,
+                  "ns_per_mma": ms * 1e6 / iters})
+    if "cvt" in which:
+        out = torch.zeros(sms * 8 * 256, dtype=torch.int32, device=dev)
+        for cps in (2, 4, 8):
+            iters = 4000
+            ms = timed(lambda: L.micro_cvt(sms * cps, iters, out.data_ptr(), sp))
+            n = sms * cps * 256 * iters * 8
+            emit({"micro": "cvt.rn.f16x2.e4m3x2", "threads_per_sm": cps * 256, "ms": ms,
+                  "per_ns_per_sm": n / (ms * 1e6) / sms})
+    if "sf_layout" in which:
+        rng = np.random.default_rng(3)
+        xa = rng.integers(120, 135, (128, 4)).astype(np.uint8)
+        xb = rng.integers(120, 135, (128, 4)).astype(np.uint8)
+        ta = np.zeros((128, 8, 4), np.uint8)
+        tb = np.zeros((128, 8, 4), np.uint8)
+        for p in range(4):
+            for r in range(128):
+                ta[32 * p + r % 32, r // 32] = xa[r]
+                tb[32 * p + r % 32, r // 32] = xb[r]
+        sa = torch.from_numpy(ta.view(np.uint32).reshape(-1).copy()).to(dev)
+        sb = torch.from_numpy(tb.view(np.uint32).reshape(-1).copy()).to(dev)
+        out = torch.zeros(128 * 128, dtype=torch.float32, device=dev)
+        for a_id, b_id in ((0, 0), (1, 2), (3, 1), (2, 3)):
+            assert L.micro_sf_layout(sa.data_ptr(), sb.data_ptr(), a_id, b_id, out.data_ptr(), err.data_ptr(), sp) == 0
+            torch.cuda.synchronize()
+            d = out.cpu().numpy().reshape(128, 128)
+            h = 32.0 * np.exp2(xa[:, a_id].astype(np.float64) - 127)[:, None] * \
+                np.exp2(xb[:, b_id].astype(np.float64) - 127)[None, :]
+            emit({"micro": "sf_layout", "a_sf_id": a_id, "b_sf_id": b_id, "layout_matches": bool(np.array_equal(d, h))})
+    torch.cuda.synchronize()
+    emit({"micro": "device_errors", "value": int(err.item())})
+
+
+if __name__ == "__main__":
+    main()
