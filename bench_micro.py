@@ -1,12 +1,15 @@
 """Microbenchmarks of the GB300 units behind the sparse path's kernel choices.
 
-    python bench_micro.py [gather] [mma] [umma] [cvt] [sf_layout]   (default: all)
+    python bench_micro.py [gather] [churn] [mma] [umma] [cvt] [sf_layout]   (default: all)
 
 Prints one JSON line per measurement (CUDA events on the launching stream,
 best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
   gather     GB/s of a 4 KB page-pair gather by 1-D TMA into shared memory,
              from a pool that fits L2 (16..128 MB) or does not (1 GB): the
              data-movement ceiling of an attention over selected pages
+  churn      the same HBM gather with the bytes spread over many short CTAs
+             (4..128 pages each): what a CTA's start and end cost in
+             bandwidth
   mma        TFLOP/s of mma.sync m16n8k16 f16 and m16n8k32 e4m3
   umma       TFLOP/s of tcgen05.mma (one issuing thread, M = 128) by N, and
              with N = 16 into several independent accumulators
@@ -42,7 +45,8 @@ def build():
 
 
 def main():
-    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "mma", "umma", "cvt", "sf_layout"]
+    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "churn", "mma", "umma", "cvt",
+                                                                    "sf_layout"]
     L = C.CDLL(build())
     vp, i32 = C.c_void_p, C.c_int
     L.micro_gather.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
@@ -87,6 +91,20 @@ def main():
                 emit({"micro": "gather", "pool_MB": nblocks * 32768 / 2 ** 20, "rows": rows, "pages_per_row": 128,
                       "ring": ring, "ms": ms, "GB_per_s": rows * 128 * 4096 / (ms / 1e3) / 1e9})
             del pool
+    if "churn" in which:  # the same bytes from HBM by many short CTAs instead of fewer long ones
+        rng = np.random.default_rng(1)
+        nblocks = 32768
+        pool = torch.zeros(nblocks * 32768, dtype=torch.uint8, device=dev)
+        for rows, ppr in ((16384, 128), (65536, 32), (262144, 8), (524288, 4)):
+            ids = torch.from_numpy((rng.integers(0, nblocks, (rows, ppr)) * 16 +
+                                    rng.integers(0, 8, (rows, ppr))).astype(np.int32)).to(dev)
+            sink = torch.zeros(rows * 128, dtype=torch.int32, device=dev)
+            for ring in (2,):
+                ms = timed(lambda: L.micro_gather(pool.data_ptr(), ids.data_ptr(), rows, ppr, ring, sink.data_ptr(),
+                                                  err.data_ptr(), sp))
+                emit({"micro": "gather_churn", "pool_MB": nblocks * 32768 / 2 ** 20, "rows": rows,
+                      "pages_per_row": ppr, "ring": ring, "ms": ms, "GB_per_s": rows * ppr * 4096 / (ms / 1e3) / 1e9})
+        del pool
     if "mma" in which:
         out = torch.zeros(sms * 8 * 256, dtype=torch.float32, device=dev)
         for e4m3 in (0, 1):

@@ -146,10 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int page_end = min((kb0 + kKeyBlocksPerCta) * kPagesPerSide, p.max_pages);
   const int seq = s_seq;
 
-  if (ntiles == 0) {
-    if (row_ok && first_epi)
-      for (int pg = kb0 * kPagesPerSide; pg < page_end; ++pg)
-        p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
+  if (ntiles == 0) {  // nothing of this key range below the tile's longest row
+    fill_neg_inf(p.scores, p.max_pages, tok0, tok1, kb0 * kPagesPerSide, page_end);
     return;
   }
 
@@ -270,10 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // pages of this key range that no tile covered
-    if (row_ok && first_epi)
-      for (int pg = (kb0 + ntiles) * kPagesPerSide; pg < page_end; ++pg)
-        p.scores[static_cast<int64_t>(tok) * p.max_pages + pg] = -INFINITY;
   }
 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -282,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
   }
+  // pages of this key range past every tile (beyond the tile's longest row)
+  fill_neg_inf(p.scores, p.max_pages, tok0, tok1, (kb0 + ntiles) * kPagesPerSide, page_end);
 }
 
 }  // namespace

@@ -153,6 +153,17 @@ __device__ __forceinline__ void tmem_ld8x4(uint32_t taddr, uint32_t stride, floa
     for (int i = 0; i < 8; ++i) v[g][i] = __uint_as_float(r[g][i]);
 }
 
+// -inf into scores[tok * max_pages + pg] for tok0 <= tok < tok1 and
+// pg0 <= pg < pg1, by the whole CTA: a warp per row at a time, its lanes along
+// the row's pages (coalesced stores)
+__device__ __forceinline__ void fill_neg_inf(float* scores, int max_pages, int tok0, int tok1, int pg0, int pg1) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int t = tok0 + warp; t < tok1; t += nwarps) {
+    float* row = scores + static_cast<int64_t>(t) * max_pages;
+    for (int pg = pg0 + lane; pg < pg1; pg += 32) row[pg] = -INFINITY;
+  }
+}
+
 // ---- host: tensor maps -------------------------------------------------------
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
