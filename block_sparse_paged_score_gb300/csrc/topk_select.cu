@@ -319,6 +319,22 @@ __global__ void __launch_bounds__(NT) topk_cta_kernel(TopkParams p) {
     pdl_wait();  // scores (and the row lengths) come from earlier kernels
     pdl_trigger();
   }
+  // a row much shorter than the kernel's width (an early prefill chunk in a
+  // batch sized for the longest row) runs with fewer keys a thread: its
+  // per-key work is then not spent on pages past its length
+  const int n = (min(max(p.row_len[blockIdx.x], 0), p.max_pages * kPage) + kPage - 1) / kPage;
+  if constexpr (KPT >= 16) {
+    if (n <= NT * (KPT / 4)) {
+      select_row_cta<KPT / 4, NT, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
+      return;
+    }
+  }
+  if constexpr (KPT >= 8) {
+    if (n <= NT * (KPT / 2)) {
+      select_row_cta<KPT / 2, NT, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
+      return;
+    }
+  }
   select_row_cta<KPT, NT, false>(p, blockIdx.x, s_hist, s_warp, s_digit, s_above, in_step);
 }
 
