@@ -5,6 +5,10 @@
 //               1-D TMA bulk copies into per-warp shared-memory rings, from
 //               a pool that fits L2 or one that does not: the data-movement
 //               ceiling of an attention that reads selected pages
+//   stream      read-only streams over a 4 GB pool, every byte once: plain
+//               16-byte loads, 4 KB page pairs by the gather kernel, and
+//               whole 16.5 KB chunks through a CTA ring (thread 0 copies,
+//               the CTA syncs per chunk)
 //   mma_sync    legacy warp MMA rates: m16n8k16 f16 and m16n8k32 e4m3
 //   umma        tcgen05.mma rate from one issuing thread, M = 128 and N =
 //               16 ... 256 (kind::f16, K = 16; kind::f8f6f4 e4m3, K = 32),
@@ -56,6 +60,57 @@ __global__ void __launch_bounds__(128) gather_kernel(const uint8_t* pool, const 
       issue(rid[warp + 4 * (i + R)], ring + st * 4096, &wb[st]);
     }
     if (++st == R) st = 0, ph ^= 1;
+  }
+  sink[static_cast<int64_t>(blockIdx.x) * 128 + tid] = acc;
+}
+
+// Read-only streams that touch every byte of the pool once (no L2 reuse):
+// plain 16-byte loads in a grid-stride loop, four in flight per thread
+__global__ void __launch_bounds__(256) stream_ld_kernel(const uint4* pool, int64_t n16, uint32_t* sink) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint32_t acc = 0;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcs(pool + i), b = __ldcs(pool + i + stride), c = __ldcs(pool + i + 2 * stride),
+                d = __ldcs(pool + i + 3 * stride);
+    acc ^= a.x ^ b.y ^ c.z ^ d.w;
+  }
+  for (; i < n16; i += stride) acc ^= __ldcs(pool + i).x;
+  sink[static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x] = acc;
+}
+
+// whole chunks (one bulk copy each, issued by thread 0) through a CTA ring
+// of S stages; every warp waits for the stage, the CTA syncs, thread 0
+// refills it: a streaming scorer's data movement without its arithmetic
+__global__ void __launch_bounds__(128) chunk_kernel(const uint8_t* pool, const int32_t* ids, int chunks_per_cta,
+                                                    int chunk, int S, uint32_t* sink, int32_t* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * chunk);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int32_t* cid = ids + static_cast<int64_t>(blockIdx.x) * chunks_per_cta;
+  auto issue = [&](int i) {
+    const int st = i % S;
+    mbar_arrive_expect_tx(&bars[st], chunk);
+    bulk_g2s(smem + st * chunk, pool + static_cast<int64_t>(cid[i]) * chunk, chunk, &bars[st]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < S && i < chunks_per_cta; ++i) issue(i);
+  uint32_t acc = 0;
+  bool alive = true;
+  for (int i = 0; i < chunks_per_cta; ++i) {
+    const int st = i % S;
+    if (alive) alive = mbar_wait(&bars[st], (i / S) & 1, err);
+    acc ^= *reinterpret_cast<const uint32_t*>(smem + st * chunk + tid * 4);
+    __syncthreads();
+    if (tid == 0 && i + S < chunks_per_cta) {
+      fence_proxy_async();
+      issue(i + S);
+    }
   }
   sink[static_cast<int64_t>(blockIdx.x) * 128 + tid] = acc;
 }
@@ -301,6 +356,23 @@ int micro_gather(const void* pool, const int32_t* ids, int rows, int pages_per_r
   switch (ring) {
     G(2) G(3) G(4) G(6) default : return -1;
   }
+  return cudaGetLastError();
+}
+
+int micro_stream_ld(const void* pool, int64_t bytes, int ctas, uint32_t* sink, cudaStream_t s) {
+  stream_ld_kernel<<<ctas, 256, 0, s>>>(static_cast<const uint4*>(pool), bytes / 16, sink);
+  return cudaGetLastError();
+}
+
+int micro_chunk(const void* pool, const int32_t* ids, int ctas, int chunks_per_cta, int chunk, int stages,
+                uint32_t* sink, int32_t* err, cudaStream_t s) {
+  if (chunk % 16 || chunk < 512 || stages < 1) return -1;
+  const int smem = stages * chunk + stages * 8;
+  if (smem > 227 * 1024) return -1;
+  cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e) return e;
+  chunk_kernel<<<ctas, 128, smem, s>>>(static_cast<const uint8_t*>(pool), ids, chunks_per_cta, chunk, stages, sink,
+                                        err);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
 """Microbenchmarks of the GB300 units behind the sparse path's kernel choices.
 
-    python bench_micro.py [gather] [churn] [mma] [umma] [cvt] [sf_layout]   (default: all)
+    python bench_micro.py [gather] [churn] [stream] [mma] [umma] [cvt] [sf_layout]   (default: all)
 
 Prints one JSON line per measurement (CUDA events on the launching stream,
 best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
@@ -10,6 +10,10 @@ best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
   churn      the same HBM gather with the bytes spread over many short CTAs
              (4..128 pages each): what a CTA's start and end cost in
              bandwidth
+  stream     GB/s of read-only streams over a 4 GB pool, every byte read
+             once (nothing for L2 to serve): plain 16-byte loads, the page
+             gather above on a permutation, and whole 16896-byte chunks (an
+             fp8 index field) through a CTA ring of 1, 2 or 4 stages
   mma        TFLOP/s of mma.sync m16n8k16 f16 and m16n8k32 e4m3
   umma       TFLOP/s of tcgen05.mma (one issuing thread, M = 128) by N, and
              with N = 16 into several independent accumulators
@@ -45,12 +49,14 @@ def build():
 
 
 def main():
-    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "churn", "mma", "umma", "cvt",
-                                                                    "sf_layout"]
+    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "churn", "stream", "mma", "umma",
+                                                                    "cvt", "sf_layout"]
     L = C.CDLL(build())
     vp, i32 = C.c_void_p, C.c_int
     L.micro_gather.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     L.micro_mma_sync.argtypes = [i32, i32, vp, i32, vp]
+    L.micro_stream_ld.argtypes = [vp, C.c_int64, i32, vp, vp]
+    L.micro_chunk.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.micro_umma.argtypes = [i32, i32, i32, i32, vp, vp, vp]
     L.micro_umma_multi.argtypes = [i32, i32, i32, vp, vp, vp]
     L.micro_cvt.argtypes = [i32, i32, vp, vp]
@@ -105,6 +111,39 @@ def main():
                 emit({"micro": "gather_churn", "pool_MB": nblocks * 32768 / 2 ** 20, "rows": rows,
                       "pages_per_row": ppr, "ring": ring, "ms": ms, "GB_per_s": rows * ppr * 4096 / (ms / 1e3) / 1e9})
         del pool
+    if "stream" in which:  # every byte of a 4 GB pool read once
+        rng = np.random.default_rng(2)
+        pool_bytes = 4 << 30
+        pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+        sink = torch.zeros(sms * 32 * 256, dtype=torch.int32, device=dev)
+        for per_sm in (4, 8, 16, 32):
+            ms = timed(lambda: L.micro_stream_ld(pool.data_ptr(), pool_bytes, sms * per_sm, sink.data_ptr(), sp))
+            emit({"micro": "stream_ld", "pool_MB": pool_bytes >> 20, "ctas_per_sm": per_sm, "threads": 256,
+                  "ms": ms, "GB_per_s": pool_bytes / (ms / 1e3) / 1e9})
+        # page pairs (block * 16 + j, j < 8, and its partner 8 slots on) in a random order, each once
+        nblk = pool_bytes // 32768
+        ids = torch.from_numpy(rng.permutation(nblk * 8).astype(np.int64)).to(dev)
+        ids = (ids // 8 * 16 + ids % 8).to(torch.int32)
+        rows = nblk * 8 // 128
+        gsink = torch.zeros(rows * 128, dtype=torch.int32, device=dev)
+        for ring in (2, 4):
+            ms = timed(lambda: L.micro_gather(pool.data_ptr(), ids.data_ptr(), rows, 128, ring, gsink.data_ptr(),
+                                              err.data_ptr(), sp))
+            emit({"micro": "stream_gather", "pool_MB": pool_bytes >> 20, "rows": rows, "pages_per_row": 128,
+                  "ring": ring, "ms": ms, "GB_per_s": rows * 128 * 4096 / (ms / 1e3) / 1e9})
+        del ids, gsink
+        chunk = 16896
+        nchunk = pool_bytes // chunk
+        perm = torch.from_numpy(rng.permutation(nchunk).astype(np.int32)).to(dev)
+        for cpc in (2, 4, 16):
+            ctas = nchunk // cpc
+            csink = torch.zeros(ctas * 128, dtype=torch.int32, device=dev)
+            for st in (1, 2, 4):
+                ms = timed(lambda: L.micro_chunk(pool.data_ptr(), perm.data_ptr(), ctas, cpc, chunk, st,
+                                                 csink.data_ptr(), err.data_ptr(), sp))
+                emit({"micro": "stream_chunk", "chunk_bytes": chunk, "chunks_per_cta": cpc, "stages": st,
+                      "ctas": ctas, "ms": ms, "GB_per_s": ctas * cpc * chunk / (ms / 1e3) / 1e9})
+        del pool, perm
     if "mma" in which:
         out = torch.zeros(sms * 8 * 256, dtype=torch.float32, device=dev)
         for e4m3 in (0, 1):

@@ -9,8 +9,8 @@
 // Work unit: one CTA per (query group, index head, chunk of 128-token
 // blocks).  A query group is q_group consecutive tokens of one sequence (the
 // decode query length), so the index cache of a sequence is read once per
-// group.  The chunk length is planned from the kernel's occupancy so that
-// the grid runs in whole waves of resident CTAs.  Thread 0 streams whole
+// group.  The chunk length is planned from the kernel's occupancy, trading
+// each CTA's fixed start against the grid's tail.  Thread 0 streams whole
 // index fields (16896 B fp8, 32768 B bf16, 8704 B MXFP4 per block and head)
 // into a shared-memory ring with 1-D TMA bulk copies completing on
 // mbarriers; the four warps each score 32 tokens of a block (two 16-token
@@ -35,21 +35,27 @@ namespace bsp {
 
 namespace {
 
+// Per format: the index field of one block and head, a key row's bytes,
+// where the per-token scales start in the field (0: none), and the deepest
+// ring the plan may give a CTA.
 template <int KEY>
 struct KeyFmt;
 template <>
 struct KeyFmt<BSP_BF16> {
-  static constexpr int kField = kBf16IndexField;
+  static constexpr int kField = kBf16IndexField, kRow = 2 * kDim, kScaleOff = 0;
   static constexpr int kStages = 3;
 };
+// fp8 rings stop at 2 fields (6 CTAs per SM): with 3 or 4 (4 or 3 CTAs per
+// SM) the mma work of a block no longer hides behind the copies (measured
+// 117 us against 92 on the 32k-token batch)
 template <>
 struct KeyFmt<BSP_FP8_E4M3> {
-  static constexpr int kField = kFp8IndexField;
-  static constexpr int kStages = 4;
+  static constexpr int kField = kFp8IndexField, kRow = kDim, kScaleOff = kFp8IndexScaleOff;
+  static constexpr int kStages = 2;
 };
 template <>
 struct KeyFmt<BSP_MXFP4> {
-  static constexpr int kField = kMxField;
+  static constexpr int kField = kMxField, kRow = kDim / 2, kScaleOff = kMxScaleOff;
   static constexpr int kStages = 6;
 };
 // fp8 keys scored against an e4m3 query: the fp8 mma takes the cached bytes
@@ -57,8 +63,8 @@ struct KeyFmt<BSP_MXFP4> {
 constexpr int kFp8KeysE4m3Q = 3;
 template <>
 struct KeyFmt<kFp8KeysE4m3Q> {
-  static constexpr int kField = kFp8IndexField;
-  static constexpr int kStages = 4;
+  static constexpr int kField = kFp8IndexField, kRow = kDim, kScaleOff = kFp8IndexScaleOff;
+  static constexpr int kStages = 2;
 };
 template <int KEY>
 constexpr int smem_bytes(int stages) {
@@ -84,6 +90,119 @@ __device__ __forceinline__ void load_q4(const void* q, int q_dtype, int64_t off,
     const uint32_t w = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(q) + off);
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = e4m3_to_float(w >> (8 * i));
+  }
+}
+
+// B fragments of the group's query rows tok0 .. tok0+ntok-1 (index head h):
+// thread (g, t) holds row g's dims in the permutation frag_dim / the fp8 mma
+// uses; columns past the group are zero.
+template <int KEY>
+__device__ __forceinline__ void load_qb(const IndexScoreParams& p, int tok0, int ntok, int h, int g, int t,
+                                        uint32_t (&qb)[8][2]) {
+  if (KEY == kFp8KeysE4m3Q) {
+    // mma m (< 4): this thread's 16-dim chunk c = t + 4*(m/2), dims 8*(m%2) + 0..7
+    const uint8_t* qrow = static_cast<const uint8_t*>(p.q) + (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int d = 16 * (t + 4 * (m >> 1)) + 8 * (m & 1);
+      qb[m][0] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
+      qb[m][1] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d + 4) : 0u;
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    if (KEY == kFp8KeysE4m3Q) break;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (g < ntok) load_q4(p.q, p.q_dtype, (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim + frag_dim<KEY>(m, t), v);
+    if (KEY == BSP_BF16) {
+      qb[m][0] = pack_bf16x2(v[0], v[1]);
+      qb[m][1] = pack_bf16x2(v[2], v[3]);
+    } else {
+      qb[m][0] = pack_f16x2(v[0], v[1]);
+      qb[m][1] = pack_f16x2(v[2], v[3]);
+    }
+  }
+}
+
+// Scores of one 16-key tile against the group's query columns (mma C
+// layout): v0 / v1 for key g and query rows 2t / 2t+1, v2 / v3 for key g+8.
+// `rows` is the shared-memory address of the tile's first key row, `scales`
+// of its first per-key scale (fp8 and MXFP4 fields).
+template <int KEY>
+__device__ __forceinline__ void tile_scores(uint32_t rows, uint32_t scales, const uint32_t (&qb)[8][2], int g, int t,
+                                            float& v0, float& v1, float& v2, float& v3) {
+  if (KEY == kFp8KeysE4m3Q) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t ra_row = rows + g * 128, rb_row = ra_row + 8 * 128;
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+      const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+      mma_e4m3(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
+      mma_e4m3(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
+    }
+    const float sg = __uint_as_float(lds32(scales + g * 4));
+    const float sg8 = __uint_as_float(lds32(scales + (g + 8) * 4));
+    v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
+  } else if (KEY == BSP_FP8_E4M3) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t ra_row = rows + g * 128, rb_row = ra_row + 8 * 128;
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+      const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+      const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2_scaled(wa[j], a0, a2);
+        e4m3x4_to_f16x2_scaled(wb[j], a1, a3);
+        mma_f16(acc, a0, a1, a2, a3, qb[4 * ii + j][0], qb[4 * ii + j][1]);
+      }
+    }
+    // per-token scale; the f16 keys hold value * 2^-8
+    const float sg = __uint_as_float(lds32(scales + g * 4)) * 256.f;
+    const float sg8 = __uint_as_float(lds32(scales + (g + 8) * 4)) * 256.f;
+    v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
+  } else if (KEY == BSP_MXFP4) {
+    float acc[4][4];
+#pragma unroll
+    for (int G = 0; G < 4; ++G) acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+    const uint32_t ra_row = rows + g * 64, rb_row = ra_row + 8 * 64;
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      const uint32_t wa = lds32(ra_row + 16 * G + 4 * t), wb = lds32(rb_row + 16 * G + 4 * t);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t a0 = e2m1x2_to_f16x2((wa >> (16 * hh)) & 0xFF);
+        const uint32_t a2 = e2m1x2_to_f16x2((wa >> (16 * hh + 8)) & 0xFF);
+        const uint32_t a1 = e2m1x2_to_f16x2((wb >> (16 * hh)) & 0xFF);
+        const uint32_t a3 = e2m1x2_to_f16x2((wb >> (16 * hh + 8)) & 0xFF);
+        mma_f16(acc[G], a0, a1, a2, a3, qb[2 * G + hh][0], qb[2 * G + hh][1]);
+      }
+    }
+    const uint32_t sa = lds32(scales + g * 4);
+    const uint32_t sb = lds32(scales + (g + 8) * 4);
+    v0 = v1 = v2 = v3 = 0.f;
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      const float ca = e8m0_to_float((sa >> (8 * G)) & 0xFF), cb = e8m0_to_float((sb >> (8 * G)) & 0xFF);
+      v0 = fmaf(acc[G][0], ca, v0);
+      v1 = fmaf(acc[G][1], ca, v1);
+      v2 = fmaf(acc[G][2], cb, v2);
+      v3 = fmaf(acc[G][3], cb, v3);
+    }
+  } else {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t ra_row = rows + g * 256, rb_row = ra_row + 8 * 256;
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
+      const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
+      mma_bf16(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
+      mma_bf16(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
+    }
+    v0 = acc[0], v1 = acc[1], v2 = acc[2], v3 = acc[3];
   }
 }
 
@@ -192,29 +311,7 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
 
   // B fragments: query row g of the group (zero beyond the group)
   uint32_t qb[8][2];
-  if (KEY == kFp8KeysE4m3Q) {
-    // mma m (< 4): this thread's 16-dim chunk c = t + 4*(m/2), dims 8*(m%2) + 0..7
-    const uint8_t* qrow = static_cast<const uint8_t*>(p.q) + (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int d = 16 * (t + 4 * (m >> 1)) + 8 * (m & 1);
-      qb[m][0] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d) : 0u;
-      qb[m][1] = g < ntok ? *reinterpret_cast<const uint32_t*>(qrow + d + 4) : 0u;
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    if (KEY == kFp8KeysE4m3Q) break;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (g < ntok) load_q4(p.q, p.q_dtype, (static_cast<int64_t>(tok0 + g) * p.hidx + h) * kDim + frag_dim<KEY>(m, t), v);
-    if (KEY == BSP_BF16) {
-      qb[m][0] = pack_bf16x2(v[0], v[1]);
-      qb[m][1] = pack_bf16x2(v[2], v[3]);
-    } else {
-      qb[m][0] = pack_f16x2(v[0], v[1]);
-      qb[m][1] = pack_f16x2(v[2], v[3]);
-    }
-  }
+  load_qb<KEY>(p, tok0, ntok, h, g, t, qb);
   const int len_lo = s_len[min(2 * t, 7)], len_hi = s_len[min(2 * t + 1, 7)];
 
   for (int i = 0; i < nb; ++i) {
@@ -226,80 +323,8 @@ __global__ void __launch_bounds__(128) index_score_kernel(IndexScoreParams p) {
     for (int tile = 0; tile < 2; ++tile) {
       const int tokb = 32 * warp + 16 * tile;
       float v0, v1, v2, v3;
-      if (KEY == kFp8KeysE4m3Q) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ra_row = sbase + (tokb + g) * 128, rb_row = ra_row + 8 * 128;
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
-          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
-          mma_e4m3(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
-          mma_e4m3(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
-        }
-        const float sg = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g) * 4);
-        const float sg8 = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g + 8) * 4);
-        v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
-      } else if (KEY == BSP_FP8_E4M3) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ra_row = sbase + (tokb + g) * 128, rb_row = ra_row + 8 * 128;
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
-          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
-          const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t a0, a1, a2, a3;
-            e4m3x4_to_f16x2_scaled(wa[j], a0, a2);
-            e4m3x4_to_f16x2_scaled(wb[j], a1, a3);
-            mma_f16(acc, a0, a1, a2, a3, qb[4 * ii + j][0], qb[4 * ii + j][1]);
-          }
-        }
-        // per-token scale; the f16 keys hold value * 2^-8
-        const float sg = *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g) * 4) * 256.f;
-        const float sg8 =
-            *reinterpret_cast<const float*>(smem + st * FB + kFp8IndexScaleOff + (tokb + g + 8) * 4) * 256.f;
-        v0 = acc[0] * sg, v1 = acc[1] * sg, v2 = acc[2] * sg8, v3 = acc[3] * sg8;
-      } else if (KEY == BSP_MXFP4) {
-        float acc[4][4];
-#pragma unroll
-        for (int G = 0; G < 4; ++G) acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
-        const uint32_t ra_row = sbase + (tokb + g) * 64, rb_row = ra_row + 8 * 64;
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-          const uint32_t wa = lds32(ra_row + 16 * G + 4 * t), wb = lds32(rb_row + 16 * G + 4 * t);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t a0 = e2m1x2_to_f16x2((wa >> (16 * hh)) & 0xFF);
-            const uint32_t a2 = e2m1x2_to_f16x2((wa >> (16 * hh + 8)) & 0xFF);
-            const uint32_t a1 = e2m1x2_to_f16x2((wb >> (16 * hh)) & 0xFF);
-            const uint32_t a3 = e2m1x2_to_f16x2((wb >> (16 * hh + 8)) & 0xFF);
-            mma_f16(acc[G], a0, a1, a2, a3, qb[2 * G + hh][0], qb[2 * G + hh][1]);
-          }
-        }
-        const uint32_t sa = lds32(sbase + kMxScaleOff + (tokb + g) * 4);
-        const uint32_t sb = lds32(sbase + kMxScaleOff + (tokb + g + 8) * 4);
-        v0 = v1 = v2 = v3 = 0.f;
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-          const float ca = e8m0_to_float((sa >> (8 * G)) & 0xFF), cb = e8m0_to_float((sb >> (8 * G)) & 0xFF);
-          v0 = fmaf(acc[G][0], ca, v0);
-          v1 = fmaf(acc[G][1], ca, v1);
-          v2 = fmaf(acc[G][2], cb, v2);
-          v3 = fmaf(acc[G][3], cb, v3);
-        }
-      } else {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ra_row = sbase + (tokb + g) * 256, rb_row = ra_row + 8 * 256;
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii) {
-          const uint4 ra = lds128(ra_row + 16 * (t + 4 * ii));
-          const uint4 rb = lds128(rb_row + 16 * (t + 4 * ii));
-          mma_bf16(acc, ra.x, rb.x, ra.y, rb.y, qb[2 * ii][0], qb[2 * ii][1]);
-          mma_bf16(acc, ra.z, rb.z, ra.w, rb.w, qb[2 * ii + 1][0], qb[2 * ii + 1][1]);
-        }
-        v0 = acc[0], v1 = acc[1], v2 = acc[2], v3 = acc[3];
-      }
+      tile_scores<KEY>(sbase + tokb * KeyFmt<KEY>::kRow, sbase + KeyFmt<KEY>::kScaleOff + tokb * 4, qb, g, t, v0, v1, v2,
+                       v3);
       // mask tokens past each row's length, then the page max over 16 tokens
       const int pos = blk_pos + tokb + g;
       float m_lo = fmaxf(pos < len_lo ? v0 : -INFINITY, pos + 8 < len_lo ? v2 : -INFINITY);
@@ -354,29 +379,28 @@ int occupancy_key(int stages) {
   });
 }
 
-// Blocks per CTA (cb) and ring depth.  Each CTA pays a fixed start (row
-// lengths, block ids, the first copy) that costs about as long as streaming
-// kStartBytes; CTAs run in waves of `resident`.  The plan minimises
-// waves * (cb + kStartBytes / field bytes) over cb = 1..32 -- whole waves,
-// without splitting a sequence's blocks finer than it pays for.  The start
-// is a time, so it is worth more of the small MXFP4 fields than of the fp8
-// ones.  The ring holds min(cb, kStages) fields, so a one-block CTA needs one
-// stage and packs more CTAs per SM.  `max_blocks` counts every group at the
-// batch's longest context; CTAs past a shorter sequence only write -inf and
-// retire at once.
-constexpr double kStartBytes = 1.5 * kFp8IndexField;
+// Blocks per CTA (cb) and ring depth.  With W blocks per SM and `occ`
+// resident CTAs per SM sharing its bandwidth, the plan minimises
+//   W * (1 + s / cb) + occ * cb / 2
+// over cb = 1..32: every CTA pays a fixed start (row lengths, block ids, the
+// first copy) worth about s blocks of streaming, and the grid ends in a tail
+// of about half a CTA, whose blocks each take occ block-times.  s is a time
+// (kStartBytes of streaming), so it is worth more of the small MXFP4 fields
+// than of the fp8 ones.  The ring holds min(cb, kStages) fields.  On a
+// 128-sequence, 32k-token batch (256 fp8 blocks per sequence) this picks
+// cb = 6: measured 91.8 us, against 92.3 at cb = 4, 93.6 at 8, 92.8 at 12,
+// 101.5 at 16 and 96.5 at 2 (the wave-count plan before it).
+constexpr double kStartBytes = 0.5 * kFp8IndexField;
 
 template <int KEY, int SEL>
 void plan_key(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
-  const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
-  const double start_blocks = kStartBytes / KeyFmt<KEY>::kField;
+  const double W = static_cast<double>(p.num_groups) * p.hidx * max_blocks / num_sms;
+  const double s = kStartBytes / KeyFmt<KEY>::kField;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {
     const int stages = std::min(cb, KeyFmt<KEY>::kStages);
-    const int64_t resident = static_cast<int64_t>(occupancy_key<KEY, SEL>(stages)) * num_sms;
-    const int64_t ctas = units * ((max_blocks + cb - 1) / cb);
-    const int64_t waves = (ctas + resident - 1) / resident;
-    const double cost = static_cast<double>(waves) * (cb + start_blocks);
+    const double occ = occupancy_key<KEY, SEL>(stages);
+    const double cost = W * (1.0 + s / cb) + occ * cb / 2.0;
     if (cb == 1 || cost < best) {
       best = cost;
       p.blocks_per_chunk = cb;
@@ -413,10 +437,12 @@ bool index_score_can_select(int32_t idx_dtype, int32_t q_dtype, int32_t max_page
 }
 
 // MXFP4 keys with e4m3 queries on tcgen05: the same chunk grid, planned with
-// that kernel's occupancy and a 4-deep ring
+// that kernel's occupancy and a 4-deep ring.  Its plan counts whole waves of
+// resident CTAs, each costing (cb + s) block-times, with s the time of
+// streaming 1.5 fp8 fields.
 void plan_mx_tc(IndexScoreParams& p, int64_t max_blocks, int num_sms) {
   const int64_t units = static_cast<int64_t>(p.num_groups) * p.hidx;
-  const double start_blocks = kStartBytes / kMxField;
+  const double start_blocks = 1.5 * kFp8IndexField / kMxField;
   const int64_t resident = static_cast<int64_t>(index_score_mx_tc_occupancy()) * num_sms;
   double best = 0.0;
   for (int cb = 1; cb <= 32; ++cb) {
