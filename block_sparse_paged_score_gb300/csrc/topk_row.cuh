@@ -20,12 +20,15 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Radix select over keys held in registers by a CTA: thread t holds NK keys
-// of candidates first..first+NK-1 (valid below n_cand).  Four 8-bit passes,
-// most significant digit first, each with one shared-memory histogram (the
-// four are zeroed by the caller before its first __syncthreads) and one warp
-// scanning its 256 bins from the top, find tau, the need-th largest key, and
-// take_eq, how many keys equal to tau are taken.  Block-wide: every thread
-// of the CTA calls it.
+// of candidates first..first+NK-1 (valid below n_cand).  Up to four 8-bit
+// passes, most significant digit first, each with one shared-memory
+// histogram (the four are zeroed by the caller before its first
+// __syncthreads) and one warp scanning its 256 bins from the top, find tau,
+// the need-th largest key, and take_eq, how many keys equal to tau are taken.
+// When the bin holding the need-th key holds exactly the keys still needed,
+// every key of the bin is taken and the passes stop there: tau becomes the
+// bin's lowest key value (the digits below zero), so "key > tau, or key ==
+// tau" is exactly the bin.  Block-wide: every thread of the CTA calls it.
 template <int NK>
 __device__ __forceinline__ void radix_select_regs(const uint32_t (&key)[NK], int first, int n_cand, int need,
                                                   int (&s_hist)[4][256], uint32_t& s_digit, int& s_above, int warp,
@@ -60,7 +63,7 @@ __device__ __forceinline__ void radix_select_regs(const uint32_t (&key)[NK], int
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (run < krem && krem <= run + c[j]) {
-            s_digit = static_cast<uint32_t>(255 - 8 * lane - j);
+            s_digit = static_cast<uint32_t>(255 - 8 * lane - j) | (static_cast<uint32_t>(c[j]) << 8);
             s_above = run;
           }
           run += c[j];
@@ -68,9 +71,11 @@ __device__ __forceinline__ void radix_select_regs(const uint32_t (&key)[NK], int
       }
     }
     __syncthreads();
+    const uint32_t dc = s_digit;
     krem -= s_above;
-    prefix |= s_digit << shift;
+    prefix |= (dc & 255u) << shift;
     mask |= 255u << shift;
+    if (static_cast<int>(dc >> 8) == krem) break;  // the whole bin is taken
   }
   tau = prefix;
   take_eq = krem;
@@ -141,39 +146,58 @@ __device__ __forceinline__ void select_row_cta(const TopkParams& p, int r, int (
   }
   const float* srow = p.scores + static_cast<int64_t>(r) * p.max_pages;
   uint32_t key[KPT];
+  if (KPT % 4 == 0 && (p.max_pages & 3) == 0 && (reinterpret_cast<uintptr_t>(p.scores) & 15) == 0 &&
+      first + KPT <= n_cand) {
+    // whole 16-byte runs (the rows start 16-byte aligned)
 #pragma unroll
-  for (int j = 0; j < KPT; ++j)
-    key[j] = (radix && first + j < n_cand) ? order_key(L2_ONLY ? __ldcg(srow + first + j) : srow[first + j]) : 0u;
+    for (int j = 0; j < KPT; j += 4) {
+      const float4* a = reinterpret_cast<const float4*>(srow + first + j);
+      const float4 v = L2_ONLY ? __ldcg(a) : *a;
+      key[j] = radix ? order_key(v.x) : 0u;
+      key[j + 1] = radix ? order_key(v.y) : 0u;
+      key[j + 2] = radix ? order_key(v.z) : 0u;
+      key[j + 3] = radix ? order_key(v.w) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+      key[j] = (radix && first + j < n_cand) ? order_key(L2_ONLY ? __ldcg(srow + first + j) : srow[first + j]) : 0u;
+  }
 
   uint32_t tau = 0;
   int take_eq = 0;
   if (radix) radix_select_regs<KPT>(key, first, n_cand, need, s_hist, s_digit, s_above, warp, lane, tau, take_eq);
 
-  // (keys > tau, keys == tau) of this thread, scanned over the block in page order
-  int gt = 0, eq = 0;
+  // keys > tau and keys == tau of this thread as bit masks (bit j: page
+  // first + j), their counts scanned over the block in page order
+  static_assert(KPT <= 32, "one bit a page");
+  uint32_t gmask = 0, emask = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const bool valid = first + j < n_cand;
-    gt += valid && (all || (radix && key[j] > tau));
-    eq += valid && radix && key[j] == tau;
+    gmask |= static_cast<uint32_t>(valid && (all || (radix && key[j] > tau))) << j;
+    emask |= static_cast<uint32_t>(valid && radix && key[j] == tau) << j;
   }
-  const int before = cta_exclusive_packed((gt << 16) | eq, s_warp, warp, lane);
-  int eqr = before & 0xFFFF;
+  const int before = cta_exclusive_packed((__popc(gmask) << 16) | __popc(emask), s_warp, warp, lane);
+  const int eqr = before & 0xFFFF;  // ties in earlier threads
   int pos = (before >> 16) + min(eqr, take_eq);
-  bool tail_sel = false;
+  // the selection: every key > tau, and the ties while fewer than take_eq
+  // came before (the lower page wins)
+  uint32_t smask = none ? 0u : gmask;
+  uint32_t ties = emask;
+  for (int left = take_eq - eqr; left > 0 && ties; --left) {
+    smask |= ties & (0u - ties);  // the lowest remaining tie
+    ties &= ties - 1;
+  }
+  const bool tail_sel = first <= n - 1 && n - 1 < first + KPT && ((smask >> (n - 1 - first)) & 1u);
+  for (uint32_t m = smask; m && pos < need; m &= m - 1, ++pos) {
+    const int j = __ffs(m) - 1, pg = first + j;
+    int32_t id = ids[0];
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int pg = first + j;
-    const bool valid = pg < n_cand;
-    const bool is_eq = valid && radix && key[j] == tau;
-    const bool sel = valid && !none && (all || (radix && key[j] > tau) || (is_eq && eqr < take_eq));
-    eqr += is_eq;
-    if (sel && pos < need) {
-      ti[pos] = pg;
-      bt[pos] = ids[KPT >= kPagesPerSide ? j / kPagesPerSide : 0] + pg % kPagesPerSide;  // first % 8 == 0 there
-      ++pos;
-    }
-    if (pg == n - 1) tail_sel = sel;
+    for (int k = 1; k < NB; ++k)
+      if (j / kPagesPerSide == k) id = ids[k];
+    ti[pos] = pg;
+    bt[pos] = id + pg % kPagesPerSide;  // first % 8 == 0 when a thread spans blocks
   }
   // the owner of page n-1 finishes the row: the forced tail entry, and the
   // context length (the tail page, if selected, is the last entry)
