@@ -9,6 +9,9 @@
 //               16-byte loads, 4 KB page pairs by the gather kernel, and
 //               whole 16.5 KB chunks through a CTA ring (thread 0 copies,
 //               the CTA syncs per chunk)
+//   tma_ring    the prefill scorer's key-tile loads alone: two 16 KB boxes a
+//               tile into a ring of one CTA per SM, 2-D tensor loads with
+//               128-byte swizzle against 1-D bulk copies of the same bytes
 //   mma_sync    legacy warp MMA rates: m16n8k16 f16 and m16n8k32 e4m3
 //   umma        tcgen05.mma rate from one issuing thread, M = 128 and N =
 //               16 ... 256 (kind::f16, K = 16; kind::f8f6f4 e4m3, K = 32),
@@ -113,6 +116,47 @@ __global__ void __launch_bounds__(128) chunk_kernel(const uint8_t* pool, const i
     }
   }
   sink[static_cast<int64_t>(blockIdx.x) * 128 + tid] = acc;
+}
+
+// Key tiles as the prefill scorer loads them: each tile is two 16 KB boxes
+// (128 rows x 128 B) at block rows of the pool, into a ring of S stages of
+// one CTA; thread 0 issues, waits for the stage S tiles back and reissues.
+// mode 0: 2-D tensor loads (128-byte swizzle), mode 1: 1-D bulk copies of
+// the same 16 KB.
+__global__ void __launch_bounds__(32, 1) tma_ring_kernel(const __grid_constant__ CUtensorMap map, const uint8_t* pool,
+                                                         const int32_t* rows, int tiles, int S, int mode,
+                                                         uint32_t* sink, int32_t* err) {
+  extern __shared__ uint8_t raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(S) * 32768);
+  if (threadIdx.x != 0) return;
+  for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+  mbar_fence_init();
+  const int32_t* r = rows + static_cast<int64_t>(blockIdx.x) * tiles * 2;
+  auto issue = [&](int j) {
+    const int st = j % S;
+    mbar_arrive_expect_tx(&bars[st], 32768);
+    for (int h = 0; h < 2; ++h) {
+      uint8_t* dst = ring + static_cast<size_t>(st) * 32768 + h * 16384;
+      if (mode == 0)
+        tma_load_2d(dst, &map, 0, r[2 * j + h], &bars[st]);
+      else
+        bulk_g2s(dst, pool + static_cast<int64_t>(r[2 * j + h]) * 128, 16384, &bars[st]);
+    }
+  };
+  for (int j = 0; j < S && j < tiles; ++j) issue(j);
+  uint32_t acc = 0;
+  bool alive = true;
+  for (int j = 0; j < tiles; ++j) {
+    const int st = j % S;
+    if (alive) alive = mbar_wait(&bars[st], (j / S) & 1, err);
+    acc ^= *reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(st) * 32768 + (j & 63) * 4);
+    if (j + S < tiles) {
+      fence_proxy_async();
+      issue(j + S);
+    }
+  }
+  sink[blockIdx.x] = acc;
 }
 
 __global__ void __launch_bounds__(256) mma_sync_kernel(int iters, float* out) {
@@ -373,6 +417,18 @@ int micro_chunk(const void* pool, const int32_t* ids, int ctas, int chunks_per_c
   if (e) return e;
   chunk_kernel<<<ctas, 128, smem, s>>>(static_cast<const uint8_t*>(pool), ids, chunks_per_cta, chunk, stages, sink,
                                         err);
+  return cudaGetLastError();
+}
+
+int micro_tma_ring(const void* pool, int64_t bytes, const int32_t* rows, int ctas, int tiles, int stages, int mode,
+                   uint32_t* sink, int32_t* err, cudaStream_t s) {
+  if (stages < 1 || stages > 6) return -1;
+  CUtensorMap map;
+  if (!make_map_u8(&map, pool, static_cast<uint64_t>(bytes / 128))) return -2;
+  const int smem = 1024 + stages * 32768 + stages * 8;
+  cudaError_t e = cudaFuncSetAttribute(tma_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e) return e;
+  tma_ring_kernel<<<ctas, 32, smem, s>>>(map, static_cast<const uint8_t*>(pool), rows, tiles, stages, mode, sink, err);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
 """Microbenchmarks of the GB300 units behind the sparse path's kernel choices.
 
-    python bench_micro.py [gather] [churn] [stream] [mma] [umma] [cvt] [sf_layout]   (default: all)
+    python bench_micro.py [gather] [churn] [stream] [tma_ring] [mma] [umma] [cvt] [sf_layout]   (default: all)
 
 Prints one JSON line per measurement (CUDA events on the launching stream,
 best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
@@ -14,6 +14,10 @@ best of 5 after a warm-up).  See bench_micro.cu for what each one runs:
              once (nothing for L2 to serve): plain 16-byte loads, the page
              gather above on a permutation, and whole 16896-byte chunks (an
              fp8 index field) through a CTA ring of 1, 2 or 4 stages
+  tma_ring   bytes per SM clock of the fp8 prefill scorer's key loads alone
+             (two 16 KB boxes a tile, a 4- or 6-stage ring, one CTA per SM)
+             from a pool that fits L2 (32 MB) or not (2 GB): 2-D tensor loads
+             with 128-byte swizzle against 1-D bulk copies
   mma        TFLOP/s of mma.sync m16n8k16 f16 and m16n8k32 e4m3
   umma       TFLOP/s of tcgen05.mma (one issuing thread, M = 128) by N, and
              with N = 16 into several independent accumulators
@@ -49,14 +53,15 @@ def build():
 
 
 def main():
-    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "churn", "stream", "mma", "umma",
-                                                                    "cvt", "sf_layout"]
+    which = [a for a in sys.argv[1:] if not a.startswith("-")] or ["gather", "churn", "stream", "tma_ring", "mma",
+                                                                    "umma", "cvt", "sf_layout"]
     L = C.CDLL(build())
     vp, i32 = C.c_void_p, C.c_int
     L.micro_gather.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
     L.micro_mma_sync.argtypes = [i32, i32, vp, i32, vp]
     L.micro_stream_ld.argtypes = [vp, C.c_int64, i32, vp, vp]
     L.micro_chunk.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    L.micro_tma_ring.argtypes = [vp, C.c_int64, vp, i32, i32, i32, i32, vp, vp, vp]
     L.micro_umma.argtypes = [i32, i32, i32, i32, vp, vp, vp]
     L.micro_umma_multi.argtypes = [i32, i32, i32, vp, vp, vp]
     L.micro_cvt.argtypes = [i32, i32, vp, vp]
@@ -144,6 +149,26 @@ def main():
                 emit({"micro": "stream_chunk", "chunk_bytes": chunk, "chunks_per_cta": cpc, "stages": st,
                       "ctas": ctas, "ms": ms, "GB_per_s": ctas * cpc * chunk / (ms / 1e3) / 1e9})
         del pool, perm
+    if "tma_ring" in which:  # the prefill scorer's key loads alone
+        rng = np.random.default_rng(4)
+        clk = 2.07e9
+        for pool_bytes in (32 << 20, 2 << 30):
+            pool = torch.zeros(pool_bytes, dtype=torch.uint8, device=dev)
+            blocks = pool_bytes // 16896
+            tiles = 256
+            # block b's keys start at row b * 132 (16896-byte fields seen as 128-byte rows)
+            rows = torch.from_numpy((rng.integers(0, blocks - 1, (sms, tiles * 2)) * 132).astype(np.int32)).to(dev)
+            tsink = torch.zeros(sms, dtype=torch.int32, device=dev)
+            for st in (4, 6):
+                for mode in (0, 1):
+                    ms = timed(lambda: L.micro_tma_ring(pool.data_ptr(), pool_bytes, rows.data_ptr(), sms, tiles, st,
+                                                        mode, tsink.data_ptr(), err.data_ptr(), sp))
+                    b = sms * tiles * 32768
+                    emit({"micro": "tma_ring", "pool_MB": pool_bytes >> 20, "stages": st,
+                          "copy": "2-D tensor, 128B swizzle" if mode == 0 else "1-D bulk",
+                          "ms": ms, "GB_per_s": b / (ms / 1e3) / 1e9,
+                          "bytes_per_sm_clock_at_2.07GHz": b / sms / (ms / 1e3) / clk})
+            del pool
     if "mma" in which:
         out = torch.zeros(sms * 8 * 256, dtype=torch.float32, device=dev)
         for e4m3 in (0, 1):
