@@ -127,13 +127,14 @@ def test_topk_bit_exact_on_oracle_scores(bsp, name):
     assert np.array_equal(gctx.cpu().numpy(), ctx)
 
 
-@pytest.mark.parametrize("max_pages", [100, 256, 700, 2048, 3000, 8000, 9000])
+@pytest.mark.parametrize("max_pages", [100, 256, 700, 701, 2047, 2048, 3000, 8000, 9000])
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
 def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
     """All three selectors: one warp per row up to 128 pages, one CTA with
     the keys in registers up to 8192, one CTA with the keys in shared memory
-    beyond."""
+    beyond.  Widths that are not a multiple of 4 pages (701, 2047) take the
+    CTA kernel's one-key-at-a-time score loads instead of its 16-byte ones."""
     rng = np.random.default_rng(3)
     rows = 300 if max_pages <= 4096 else 60
     sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
