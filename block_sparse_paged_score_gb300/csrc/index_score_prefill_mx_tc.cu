@@ -189,13 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(a_full, kQTile);
       tma_load_2d(sm.a, &tmap_q, 0, tok0, a_full);
       for (int j = 0; j < min(kStages, ntiles); ++j) load_b(j);
-      alive = mbar_wait(a_full, 0, p.err);
+      alive = mbar_wait_sleep(a_full, 0, p.err);
       const uint32_t a_addr = smem_u32(sm.a);
       for (int j = 0; j < ntiles && alive; ++j) {
         const int st = j % kStages, buf = j & 1;
-        alive = mbar_wait(&b_full[st], (j / kStages) & 1, p.err) &&
-                mbar_wait(&sf_full[st], (j / kStages) & 1, p.err) &&
-                mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
+        alive = mbar_wait_sleep(&b_full[st], (j / kStages) & 1, p.err) &&
+                mbar_wait_sleep(&sf_full[st], (j / kStages) & 1, p.err) &&
+                mbar_wait_sleep(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
         if (!alive) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(sm.b + st * kKeyTile);
@@ -208,11 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&acc_full[buf]);
         const int jp = j - 1;  // refill the previous tile's stage (its MMAs were issued an iteration ago)
         if (jp >= 0 && jp + kStages < ntiles) {
-          alive = mbar_wait(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
+          alive = mbar_wait_sleep(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
           if (alive) load_b(jp + kStages);
         }
       }
-      if (alive) mbar_wait(&b_empty[(ntiles - 1) % kStages], ((ntiles - 1) / kStages) & 1, p.err);
+      if (alive) mbar_wait_sleep(&b_empty[(ntiles - 1) % kStages], ((ntiles - 1) / kStages) & 1, p.err);
     }
     __syncwarp();
   } else if (warp <= kScaleWarps) {
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool alive = true;
     for (int j = 0; j < ntiles && alive; ++j) {
       const int st = j % kStages;
-      if (j >= kStages) alive = mbar_wait(&b_empty[st], ((j / kStages) - 1) & 1, p.err);  // the slot's MMAs are done
+      if (j >= kStages) alive = mbar_wait_sleep(&b_empty[st], ((j / kStages) - 1) & 1, p.err);  // the slot's MMAs are done
       if (!alive) break;
       const int bid = s_bid[j];
       uint32_t w[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};  // a missing block: zero keys, unit scales
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool alive = true;
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
-      if (alive) alive = mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
+      if (alive) alive = mbar_wait_sleep(&acc_full[buf], (j >> 1) & 1, p.err);
       if (!alive) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       float v[64];

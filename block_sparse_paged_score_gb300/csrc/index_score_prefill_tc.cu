@@ -197,12 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(a_full, kTileBytes);
       tma_load_2d(sm.a, &tmap_q, 0, tok0, a_full);
       for (int j = 0; j < min(kStages, ntiles); ++j) load_b(j);
-      mbar_wait(a_full, 0, p.err);
+      mbar_wait_sleep(a_full, 0, p.err);
       const uint32_t a_addr = smem_u32(sm.a);
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % kStages, buf = j & 1;
-        mbar_wait(&b_full[st], (j / kStages) & 1, p.err);
-        mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
+        mbar_wait_sleep(&b_full[st], (j / kStages) & 1, p.err);
+        mbar_wait_sleep(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.err);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(sm.b + st * 2 * kTileBytes);
 #pragma unroll
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ago), so the MMAs just issued queue behind them without a wait
         const int jp = j - 1;
         if (jp >= 0 && jp + kStages < ntiles) {
-          mbar_wait(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
+          mbar_wait_sleep(&b_empty[jp % kStages], (jp / kStages) & 1, p.err);
           load_b(jp + kStages);
         }
       }
@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = j & 1;
       // the tile's key scales (a missing block leaves stale but finite
       // scales: its keys lie past every row's length and are masked)
-      mbar_wait(&scale_full[j % kScaleSlots], (j / kScaleSlots) & 1, p.err);
-      mbar_wait(&acc_full[buf], (j >> 1) & 1, p.err);
+      mbar_wait_sleep(&scale_full[j % kScaleSlots], (j / kScaleSlots) & 1, p.err);
+      mbar_wait_sleep(&acc_full[buf], (j >> 1) & 1, p.err);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       float v[64];
       tmem_ld32x2(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + buf * 256 + col0, v);
