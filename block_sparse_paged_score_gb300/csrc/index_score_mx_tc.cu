@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(sm.q);
       for (int i = 0; i < nb && alive; ++i) {
         const int st = i % kStages, buf = i & 1;
-        alive = mbar_wait(&full[st], (i / kStages) & 1, p.err) &&
-                mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, p.err);
+        alive = mbar_wait_sleep(&full[st], (i / kStages) & 1, p.err) &&
+                mbar_wait_sleep(&acc_empty[buf], ((i >> 1) & 1) ^ 1, p.err);
         if (!alive) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t k_addr = smem_u32(sm.keys + st * kKeyTile);
@@ -196,13 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ago, so this wait overlaps the ones just issued
         const int j = i - 1;
         if (j >= 0 && j + kStages < nb) {
-          alive = mbar_wait(&empty[j % kStages], (j / kStages) & 1, p.err);
+          alive = mbar_wait_sleep(&empty[j % kStages], (j / kStages) & 1, p.err);
           if (alive) load_block(j + kStages);
         }
       }
       // nothing may still be writing shared memory or TMEM when the CTA
       // leaves: wait (bounded) for the last MMAs
-      if (alive && nb > 0) mbar_wait(&empty[(nb - 1) % kStages], ((nb - 1) / kStages) & 1, p.err);
+      if (alive && nb > 0) mbar_wait_sleep(&empty[(nb - 1) % kStages], ((nb - 1) / kStages) & 1, p.err);
     }
     __syncwarp();
   } else {
@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nb && alive; ++i) {
       const int buf = i & 1;
       const int ss = i % kScaleSlots;
-      alive = mbar_wait(&scale_full[ss], (i / kScaleSlots) & 1, p.err) &&
-              mbar_wait(&acc_full[buf], (i >> 1) & 1, p.err);
+      alive = mbar_wait_sleep(&scale_full[ss], (i / kScaleSlots) & 1, p.err) &&
+              mbar_wait_sleep(&acc_full[buf], (i >> 1) & 1, p.err);
       alive = __all_sync(0xffffffffu, alive);  // tcgen05.ld below is warp-wide
       if (!alive) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
