@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -68,6 +69,9 @@ def parse():
                          "at least 4x the L2 (the inputs are larger than L2), else flush")
     ap.add_argument("--select-blocks", action="store_true",
                     help="128-token blocks as the unit of selection (top_k_pages / 8 blocks a row)")
+    ap.add_argument("--decode-seqs", type=int, default=0,
+                    help="keep only the first N sequences of a decode-only workload (a smaller batch of the same "
+                         "shape, for ncu captures that must stay small); 0: all")
     return ap.parse_args()
 
 
@@ -75,12 +79,19 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
-def rank_workload_spec(config, rank):
+def rank_workload_spec(config, rank, decode_seqs=0):
     """Each rank runs its own batch: the configuration's shapes with seeds
-    offset by the rank (weak scaling; nothing is exchanged between ranks)."""
+    offset by the rank (weak scaling; nothing is exchanged between ranks).
+    decode_seqs > 0 keeps the first decode_seqs sequences of a decode-only
+    configuration, renamed after its sequence count."""
     from block_sparse_paged_score_gb300 import workloads as W
     spec = dict(W.CONFIGS[config])
     spec["seed"] = spec["seed"] + 1000 * rank
+    if decode_seqs > 0:
+        if spec.get("prefill_chunks"):
+            raise SystemExit("--decode-seqs applies to decode-only workloads")
+        spec["decode_lens"] = list(spec["decode_lens"])[:decode_seqs]
+        spec["name"] = re.sub(r"\d+seq", "%dseq" % len(spec["decode_lens"]), spec["name"])
     return spec
 
 
@@ -349,7 +360,7 @@ def run_ours(args):
     from block_sparse_paged_score_gb300 import bsp, step, workloads as W
 
     bsp.lib()
-    w = W.Workload(rank_workload_spec(args.config, rank))
+    w = W.Workload(rank_workload_spec(args.config, rank, args.decode_seqs))
 
     def t(a):
         a = np.ascontiguousarray(a)

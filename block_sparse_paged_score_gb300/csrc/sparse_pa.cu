@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(128, PaFmt<KV>::kMinCtas)
   int st = 0;         // ring slot of page i, and the parity of its phase
   uint32_t phase = 0;
   for (int i = 0; i < nw; ++i) {
-    if (alive) alive = mbar_wait(&wbar[st], phase, p.err);
+    if (alive) alive = mbar_wait_sleep(&wbar[st], phase, p.err);
     const int pg = p0 + warp + 4 * i;
     if (KV == BSP_MXFP4) {
       __syncwarp();  // every lane is done reading the previous dequantised page
