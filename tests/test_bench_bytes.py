@@ -31,3 +31,17 @@ def test_index_and_attention_bytes_of_a_batch():
     kv = ctx * 256  # fp8 K and V: 128 B each per token
     q = out = 32 * 16 * 128 * 2  # bf16 queries and output, 16 heads
     assert bench.attention_algorithmic_bytes(w, ctx) == kv + q + out
+
+
+def test_smaller_decode_batch_for_captures():
+    """--decode-seqs keeps the first N sequences of a decode-only workload
+    under a name that says so, and refuses a chunked-prefill one."""
+    full = bench.rank_workload_spec(3, 0)
+    spec = bench.rank_workload_spec(3, 0, 80)
+    assert spec["name"] == "fp8-80seq-L32k-q4" and full["name"] == "fp8-128seq-L32k-q4"
+    assert list(spec["decode_lens"]) == list(full["decode_lens"])[:80]
+    w = W.Workload(spec)
+    assert w.num_decode_rows == 80 * 4
+    assert bench.rank_workload_spec(3, 1, 80)["seed"] == full["seed"] + 1000
+    with pytest.raises(SystemExit):
+        bench.rank_workload_spec(5, 0, 8)
