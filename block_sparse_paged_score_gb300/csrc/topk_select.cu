@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkParams p) {
 constexpr int kCtaThreads = 256;
 
 template <int KPT, int NT = kCtaThreads>
-__global__ void __launch_bounds__(NT, 1024 / NT) topk_cta_kernel(TopkParams p) {
+__global__ void __launch_bounds__(NT, NT == 256 ? (KPT >= 32 ? 4 : 5) : 1024 / NT) topk_cta_kernel(TopkParams p) {
   __shared__ int s_hist[4][256];
   __shared__ int s_warp[NT / 32];
   __shared__ uint32_t s_digit;
