@@ -25,9 +25,9 @@ steps then run once more with an event between kernels, which gives each
 kernel's duration for the roofline (an upper bound: the events serialise the
 kernels).  SM clocks are sampled with nvidia-smi during both passes.  `e2e` repeats the measurement through the public step API with the
 step's inputs in pinned host memory and the attention output returned to
-pinned host memory, inside the timed region: with copy-engine copies, and (a
-decode step) zero-copy, the kernels loading and storing the pinned buffers
-over NVLink-C2C; the faster is `e2e`, both are listed.  `cpu_baseline` times the CPU oracle (C, OpenMP)
+pinned host memory, inside the timed region: with copy-engine copies, and
+zero-copy, the kernels loading and storing the pinned buffers over
+NVLink-C2C (and the two mixes); the fastest is `e2e`, all are listed.  `cpu_baseline` times the CPU oracle (C, OpenMP)
 on a bounded sample of the same workload; `--impl reference` reports that
 oracle as the reference arm.
 
@@ -486,11 +486,11 @@ def run_ours(args):
         roof = dict(kernels[dom], kernel=dom)
 
     # end to end through the public step API, inputs in pinned host memory and
-    # the output returned to pinned host memory, every step.  A decode step
-    # runs it twice: with copy-engine copies (one host-to-device copy of the
-    # packed inputs, one device-to-host copy of the output) and zero-copy (the
-    # step's kernels load the inputs from and store the output to the pinned
-    # buffers over NVLink-C2C).  `e2e` is the faster of the two; both are kept.
+    # the output returned to pinned host memory, every step: with copy-engine
+    # copies (one host-to-device copy of the packed inputs, one device-to-host
+    # copy of the output), zero-copy (the step's kernels load the inputs from
+    # and store the output to the pinned buffers over NVLink-C2C), and the two
+    # mixes.  `e2e` is the fastest; all are kept.
     e2e = None
     if not args.no_e2e:
         host = {kk: vv.cpu() for kk, vv in inputs.items()}
@@ -512,11 +512,10 @@ def run_ours(args):
             return {"value": tokens * world / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e_ms,
                     "h2d_bytes_per_step": hs.h2d_bytes, "d2h_bytes_per_step": hs.d2h_bytes}
 
-        modes = {"copy_engine": step.HostDecodeStep(st, host, device=dev)}
-        if not mixed:
-            modes["zero_copy"] = step.HostDecodeStep(st, host, device=dev, zero_copy=True)
-            modes["copy_in_zero_out"] = step.HostDecodeStep(st, host, device=dev, inputs="copy", output="zero")
-            modes["zero_in_copy_out"] = step.HostDecodeStep(st, host, device=dev, inputs="zero", output="copy")
+        modes = {"copy_engine": step.HostDecodeStep(st, host, device=dev),
+                 "zero_copy": step.HostDecodeStep(st, host, device=dev, zero_copy=True),
+                 "copy_in_zero_out": step.HostDecodeStep(st, host, device=dev, inputs="copy", output="zero"),
+                 "zero_in_copy_out": step.HostDecodeStep(st, host, device=dev, inputs="zero", output="copy")}
         res = {m: time_host(hs) for m, hs in modes.items()}
         best = max(res, key=lambda m: res[m]["value"])
         e2e = dict(res[best], transfer=best, modes=res)

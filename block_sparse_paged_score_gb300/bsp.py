@@ -119,10 +119,13 @@ def _check(fn, status):
 
 
 def _ptr(t):
+    """The device address of a CUDA tensor, or of a pinned host tensor
+    (pinned memory is mapped into the device's address space: the kernels
+    read and write it in place)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("libbsp takes CUDA tensors")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("libbsp takes CUDA tensors or pinned host tensors")
     return t.data_ptr()
 
 

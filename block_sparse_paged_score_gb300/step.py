@@ -79,15 +79,16 @@ class HostDecodeStep:
               pinned buffer, or the attention stores its output straight
               into pinned host memory (pinned memory is mapped into the
               device's address space; on a Grace-Blackwell node these loads
-              and stores cross NVLink-C2C).  A DecodeStep only.
-    zero_copy=True is inputs="zero", output="zero"."""
+              and stores cross NVLink-C2C).
+    zero_copy=True is inputs="zero", output="zero".  Works for a DecodeStep
+    and for a MixedStep."""
 
     def __init__(self, step, host_inputs, device="cuda", zero_copy=False, inputs=None, output=None):
         self.step = step
         self.inputs = inputs or ("zero" if zero_copy else "copy")
         self.output = output or ("zero" if zero_copy else "copy")
-        if "zero" in (self.inputs, self.output) and not isinstance(step, DecodeStep):
-            raise ValueError("zero-copy transfer needs a DecodeStep")
+        if "zero" in (self.inputs, self.output) and not isinstance(step, (DecodeStep, MixedStep)):
+            raise ValueError("zero-copy transfer needs a DecodeStep or a MixedStep")
         offs, total = {}, 0
         for k, v in host_inputs.items():
             offs[k] = total
@@ -117,7 +118,15 @@ class HostDecodeStep:
             if self.inputs == "copy":
                 self.dev_buf.copy_(self.host_buf, non_blocking=True)
             d = self.dev if self.inputs == "copy" else self.host
-            if self.output == "zero":
+            if self.output == "zero" and isinstance(self.step, MixedStep):
+                # the step's attention launches store into the pinned output
+                dev_out = self.step.out
+                self.step.out = self.out_host
+                try:
+                    self.step.run(d["k"], d["v"], d["idx_k"], d["slot"], d["q"], d["idx_q"], d["seq_lens"], stream=s)
+                finally:
+                    self.step.out = dev_out
+            elif self.output == "zero":
                 a = self.step.args
                 dev_out = a.out
                 a.out = self.out_host.data_ptr()

@@ -446,6 +446,31 @@ def test_host_step_zero_copy_matches_device_step(bsp, name):
             assert torch.equal(out, ref.cpu()), (inputs, output)
 
 
+def test_mixed_step_zero_copy_matches_device_step(bsp):
+    """The chunked-prefill step (decode rows, prefill chunks, a pad sequence)
+    fed straight from pinned host memory, and storing its output there,
+    equals the step on device copies bit for bit; so does the copy-engine
+    host step."""
+    from block_sparse_paged_score_gb300 import step
+    w, o, g = sides("mixed")
+    st = step.MixedStep(w, g.kv, g.idx, g.block_table)
+    k, v, ik, slot = w.step_tokens()
+    dev = {"k": g.t(k), "v": g.t(v), "idx_k": g.t(ik), "slot": g.t(slot), "q": g.q_bf16, "idx_q": g.idx_q_bf16,
+           "seq_lens": g.t(w.decode_lens)}
+    st.run(dev["k"], dev["v"], dev["idx_k"], dev["slot"], dev["q"], dev["idx_q"], dev["seq_lens"])
+    ref = st.out.clone()
+    torch.cuda.synchronize()
+    assert st.dev_err.item() == 0
+    host = {kk: vv.cpu() for kk, vv in dev.items()}
+    for inputs in ("zero", "copy"):
+        for output in ("zero", "copy"):
+            hs = step.HostDecodeStep(st, host, inputs=inputs, output=output)
+            out = hs.run()
+            torch.cuda.synchronize()
+            assert st.dev_err.item() == 0
+            assert torch.equal(out, ref.cpu()), (inputs, output)
+
+
 @pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2"])
 def test_decode_step_selection_in_scorer(bsp, name):
     """With sel_counters the scorer's last CTA of each sequence selects its
