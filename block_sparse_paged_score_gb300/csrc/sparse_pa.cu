@@ -309,13 +309,22 @@ __device__ __forceinline__ void pa_page(PaState& a, uint32_t qs, uint32_t kaddr,
         }
       }
     }
+    // only a row's last page can reach past its context; the others skip
+    // the per-token test (a warp-uniform branch)
+    if (tok0 + kPage <= ctx) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
-        s[nt][j] = tok0 + tok < ctx ? (acc[nt][0][j] + acc[nt][1][j]) * qk_scale : -INFINITY;
-      }
+        for (int j = 0; j < 4; ++j) s[nt][j] = (acc[nt][0][j] + acc[nt][1][j]) * qk_scale;
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tok = F16 ? 4 * t + 2 * nt + (j & 1) : 8 * nt + 2 * t + (j & 1);
+          s[nt][j] = tok0 + tok < ctx ? (acc[nt][0][j] + acc[nt][1][j]) * qk_scale : -INFINITY;
+        }
+    }
   }
 
   // online softmax (log2 domain); rows g (regs 0,1) and g+8 (regs 2,3)
