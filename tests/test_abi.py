@@ -71,3 +71,14 @@ def test_host_validation_without_a_gpu():
                                           None, None) == 2
     assert L.bsp_sparse_pa_decode_noalloc(C.byref(d2), fake, bsp.BF16, 32, fake, fake, 3, 8, C.c_float(0.1), fake,
                                           None, None) == 1  # rows not a multiple of the KV heads
+
+
+def test_binding_refuses_pageable_host_tensors():
+    """Tensors reach the library as device addresses: CUDA tensors, or pinned
+    host tensors (mapped into the device's address space).  A pageable host
+    tensor has no device address and is refused before any call."""
+    import torch
+    from block_sparse_paged_score_gb300 import bsp
+    assert bsp._ptr(None) is None
+    with pytest.raises(ValueError):
+        bsp._ptr(torch.empty(4))
