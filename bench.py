@@ -85,7 +85,7 @@ def rank_workload_spec(config, rank, decode_seqs=0):
     decode_seqs > 0 keeps the first decode_seqs sequences of a decode-only
     configuration, renamed after its sequence count."""
     from block_sparse_paged_score_gb300 import workloads as W
-    spec = dict(W.CONFIGS[config])
+    spec = dict(W.WORKLOADS[config])
     spec["seed"] = spec["seed"] + 1000 * rank
     if decode_seqs > 0:
         if spec.get("prefill_chunks"):

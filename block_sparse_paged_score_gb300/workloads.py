@@ -30,7 +30,7 @@ KIND_K, KIND_V, KIND_IDX, KIND_Q, KIND_IDXQ, KIND_LEN, KIND_PERM, KIND_GROUP = r
 FP8_K_SCALE = 0.0095
 FP8_V_SCALE = 0.0105
 
-CONFIGS = {
+WORKLOADS = {
     1: dict(name="tiny-bf16-L1024", seed=1001, kv_dtype=BF16, idx_dtype=BF16, q_dtype=BF16, idx_q_dtype=BF16,
             hkv=1, group=4, k_pages=16, q_len=1, decode_lens=[1024]),
     2: dict(name="fp8-32seq-L4k-8k", seed=1002, kv_dtype=FP8, idx_dtype=FP8, q_dtype=BF16, idx_q_dtype=FP8,
@@ -235,4 +235,4 @@ class Workload:
 
 
 def workload(config_id):
-    return Workload(CONFIGS[config_id])
+    return Workload(WORKLOADS[config_id])

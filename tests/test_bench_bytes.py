@@ -12,7 +12,7 @@ from block_sparse_paged_score_gb300 import workloads as W
 
 @pytest.mark.parametrize("dtype", [W.BF16, W.FP8, W.MXFP4])
 def test_bytes_per_token_are_the_layouts(dtype):
-    w = W.Workload(dict(W.CONFIGS[1], idx_dtype=dtype, kv_dtype=dtype, name="probe"))
+    w = W.Workload(dict(W.WORKLOADS[1], idx_dtype=dtype, kv_dtype=dtype, name="probe"))
     q_idx = w.num_decode_tokens * w.hidx * 128 * (2 if w.idx_q_dtype == W.BF16 else 1)
     scores = w.num_decode_tokens * w.hkv * w.max_pages * 4
     keys = int(w.decode_lens.sum()) * O.index_field_bytes(dtype) // 128 * w.hidx
