@@ -32,19 +32,19 @@
  *    one index head per KV head in the shapes this library is built for, but
  *    the index calls take their own head count.
  *  - Memory.  Every pointer to data is a DEVICE pointer unless stated; the
- *    caller owns every buffer (including workspaces).  The per-token inputs
- *    and the output, which the kernels touch once with plain loads and
- *    stores, may instead point into pinned host memory (page-locked, which
- *    unified addressing maps into the device's address space; the kernels
- *    then read and write it in place over the host link):
- *    bsp_kv_page_write's k, v, idx_k and slot; bsp_cast_e4m3's
- *    x and out; bsp_row_lengths_decode's seq_lens; the attention calls' q
- *    and out; the step inputs and out of bsp_sparse_decode_step.  Caches,
- *    block tables, score rows, selections and workspaces must be device
- *    memory (the kernels read them by TMA or more than once).  The library never
- *    allocates, never synchronises the stream and never reads device memory
- *    back to the host inside a call, so every call may be captured into a CUDA
- *    graph.  All work is enqueued on `stream` (0 = legacy default stream).
+ *    caller owns every buffer (including workspaces).  The per-token inputs and
+ *    the output, which the kernels touch once with plain loads and stores, may
+ *    instead point into pinned host memory (page-locked, which unified
+ *    addressing maps into the device's address space; the kernels then read
+ *    and write it in place over the host link): bsp_kv_page_write's k, v,
+ *    idx_k and slot; bsp_cast_e4m3's x and out; bsp_row_lengths_decode's
+ *    seq_lens; the attention calls' q and out; the step inputs and out of
+ *    bsp_sparse_decode_step.  Caches, block tables, score rows, selections and
+ *    workspaces must be device memory (the kernels read them by TMA or more
+ *    than once).  The library never allocates, never synchronises the stream
+ *    and never reads device memory back to the host inside a call, so every
+ *    call may be captured into a CUDA graph.  All work is enqueued on `stream`
+ *    (0 = legacy default stream).
  *  - Errors.  Invalid arguments are detected on the host and returned before
  *    anything is enqueued.  A failed launch returns BSP_ERR_CUDA (the CUDA
  *    error stays readable through bsp_last_cuda_error).  Data-dependent
