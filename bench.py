@@ -123,10 +123,31 @@ def measured_bf16_sustained():
     return BF16_FALLBACK_TFLOPS, "fallback"
 
 
+def kernel_sources(files):
+    """The kernel's sources and every local header they include, directly or
+    through another header (`#include "..."`), as sorted repository paths."""
+    csrc = os.path.join(ROOT, "block_sparse_paged_score_gb300", "csrc")
+    todo = [os.path.normpath(os.path.join(csrc, f)) for f in files]
+    seen = set()
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        for line in open(f):
+            m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+            if m:
+                todo.append(os.path.normpath(os.path.join(os.path.dirname(f), m.group(1))))
+    return sorted(os.path.relpath(f, ROOT) for f in seen)
+
+
 def kernel_source_hash(files):
+    """Hash of a kernel's sources and headers: a DRAM record is reported only
+    while none of them has changed since its capture."""
     h = hashlib.sha256()
-    for f in files:
-        h.update(open(os.path.join(ROOT, "block_sparse_paged_score_gb300", "csrc", f), "rb").read())
+    for f in kernel_sources(files):
+        h.update(f.encode() + b"\0")
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -452,10 +473,10 @@ def run_ours(args):
     score_s = statistics.mean(score_ms) / 1e3
     attn_s = statistics.mean(attn_ms) / 1e3
     # MXFP4 keys with e4m3 queries run the tcgen05 scorer
-    idx_kernel = (("index_score_mx_tc_kernel", ["index_score_mx_tc.cu", "tcgen05.cuh", "common.cuh"])
-                  if w.idx_dtype == 2 and w.idx_q_dtype == 1 else ("index_score_kernel", ["index_score.cu", "common.cuh"]))
+    idx_kernel = (("index_score_mx_tc_kernel", ["index_score_mx_tc.cu"])
+                  if w.idx_dtype == 2 and w.idx_q_dtype == 1 else ("index_score_kernel", ["index_score.cu"]))
     per = {"index_score": (score_bytes, score_s) + idx_kernel,
-           "sparse_pa": (attn_bytes, attn_s, "sparse_pa_kernel", ["sparse_pa.cu", "common.cuh"])}
+           "sparse_pa": (attn_bytes, attn_s, "sparse_pa_kernel", ["sparse_pa.cu"])}
     kernels = {}
     for name, (nbytes, secs, kname, files) in per.items():
         kernels[name] = {"bound": "hbm", "achieved": nbytes / secs / 1e9, "peak": peak, "unit": "GB/s",
