@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -328,16 +329,43 @@ def oracle_sample(w, seconds, blocks=False):
     return one if n == 1 else OracleStep(w, n, blocks)
 
 
-def cpu_oracle_rate(w, seconds=10.0, blocks=False):
+def cpu_oracle_rate(w, seconds=10.0, blocks=False, threads=None):
     """The oracle's rate on a sample of the workload: one warm-up pass, then
-    passes until about `seconds` have gone by (at least three)."""
+    passes until about `seconds` have gone by (at least three).  `threads`
+    (optional) limits the oracle's OpenMP loops for this measurement."""
     import oracle as O
-    o = oracle_sample(w, seconds, blocks)
-    o.run()
-    times = []
-    while len(times) < 3 or sum(times) < seconds:
-        times.append(o.run())
-    return o.tokens * len(times) / sum(times), O.num_threads(), f"{o.desc}, mean of {len(times)} passes after a warm-up"
+    before = O.num_threads()
+    if threads:
+        O.set_num_threads(threads)
+    try:
+        used = O.num_threads()
+        o = oracle_sample(w, seconds, blocks)
+        o.run()
+        times = []
+        while len(times) < 3 or sum(times) < seconds:
+            times.append(o.run())
+    finally:
+        O.set_num_threads(before)
+    return o.tokens * len(times) / sum(times), used, f"{o.desc}, mean of {len(times)} passes after a warm-up"
+
+
+def cpu_model():
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the
+    machine type)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
 
 
 # ---------------------------------------------------------------------------
@@ -361,7 +389,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_desc(w, args.select_blocks, l2_policy(w, args.l2)),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": O.num_threads(), "kind": "oracle",
-                             "sample": o.desc},
+                             "sample": o.desc, "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -544,7 +572,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, threads, desc = cpu_oracle_rate(w, blocks=args.select_blocks)
-        cpu = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = {"value": r, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "cpu_model": cpu_model()}
+        if args.config in (1, 2):
+            # the two small workloads are also timed on one core
+            r1, _, desc1 = cpu_oracle_rate(w, seconds=5.0, blocks=args.select_blocks, threads=1)
+            cpu["single_thread"] = {"value": r1, "unit": "tokens/s", "cores": 1, "sample": desc1}
 
     if rank == 0:
         line = {"metric": "sparse-decode tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -74,6 +74,8 @@ def _declare(L):
     L.orc_sparse_attention.argtypes = [i32, i32, vp, f32, f32, vp, i32, i32, vp, vp, i32, i32, f32, vp, vp, i32]
     L.orc_dense_attention.argtypes = [i32, i32, vp, f32, f32, vp, i32, i32, vp, i32, vp, vp, i32, f32, vp, vp, i32]
     L.orc_num_threads.restype = i32
+    L.orc_set_num_threads.argtypes = [i32]
+    L.orc_set_num_threads.restype = None
 
 
 def _subset(rows):
@@ -248,6 +250,11 @@ def dense_attention(kv_dtype, hkv, kv_cache, k_scale, v_scale, q, q_dtype, group
 
 def num_threads():
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n):
+    """Threads of the oracle's later OpenMP loops (for a one-core timing)."""
+    lib().orc_set_num_threads(int(n))
 
 
 def bf16_to_f32(a):

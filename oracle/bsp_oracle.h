@@ -141,6 +141,9 @@ void orc_dense_attention(int kv_dtype, int num_kv_heads, const uint8_t* kv_cache
 
 /* threads the oracle's OpenMP loops use (1 when built without OpenMP) */
 int orc_num_threads(void);
+/* sets the threads of the oracle's later OpenMP loops (n > 0; no-op without
+   OpenMP); for timing the oracle on one core */
+void orc_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

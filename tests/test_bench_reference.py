@@ -30,6 +30,7 @@ def test_reference_arm_prints_one_line_with_the_benchmark_keys():
     assert d["config"]["workload"] == "tiny-bf16-L1024"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
@@ -37,3 +38,14 @@ def test_reference_arm_other_ranks_print_nothing():
     r = _run({"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.lstrip().startswith("{")]
+
+
+def test_oracle_timed_on_one_core_then_restored():
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle as O
+    from block_sparse_paged_score_gb300 import workloads as W
+    before = O.num_threads()
+    rate, cores, desc = bench.cpu_oracle_rate(W.workload(1), seconds=0.05, threads=1)
+    assert rate > 0 and cores == 1 and desc
+    assert O.num_threads() == before
