@@ -119,9 +119,20 @@ def _check(fn, status):
 
 
 def _ptr(t):
-    """The device address of a CUDA tensor, or of a pinned host tensor
-    (pinned memory is mapped into the device's address space: the kernels
-    read and write it in place)."""
+    """The device address of a CUDA tensor: caches, tables, lengths, score
+    rows, selections and workspaces must live in device memory."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libbsp takes a CUDA tensor here (only per-token inputs and outputs may be pinned host "
+                         "tensors)")
+    return t.data_ptr()
+
+
+def _io_ptr(t):
+    """The address of a per-token input or output: a CUDA tensor, or a pinned
+    host tensor (pinned memory is mapped into the device's address space;
+    the kernels read or write it once, in place)."""
     if t is None:
         return None
     if not t.is_cuda and not t.is_pinned():
@@ -174,13 +185,14 @@ class IndexCache:
 
 def kv_page_write(kv, idx, k, v, idx_k, slot, dev_err=None, stream=None):
     _check("bsp_kv_page_write",
-           lib().bsp_kv_page_write(C.byref(kv.desc), C.byref(idx.desc) if idx is not None else None, _ptr(k), _ptr(v),
-                                   _ptr(idx_k), _ptr(slot), slot.numel(), _ptr(dev_err), _stream(stream)))
+           lib().bsp_kv_page_write(C.byref(kv.desc), C.byref(idx.desc) if idx is not None else None, _io_ptr(k),
+                                   _io_ptr(v), _io_ptr(idx_k), _io_ptr(slot), slot.numel(), _ptr(dev_err),
+                                   _stream(stream)))
 
 
 def cast_e4m3(x, out=None, stream=None):
     out = out if out is not None else torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    _check("bsp_cast_e4m3", lib().bsp_cast_e4m3(_ptr(x), _ptr(out), x.numel(), _stream(stream)))
+    _check("bsp_cast_e4m3", lib().bsp_cast_e4m3(_io_ptr(x), _io_ptr(out), x.numel(), _stream(stream)))
     return out
 
 
@@ -188,7 +200,7 @@ def row_lengths_decode(seq_lens, q_len, num_heads, row_seq=None, row_len=None, s
     rows = seq_lens.numel() * q_len * num_heads
     row_seq = row_seq if row_seq is not None else torch.empty(rows, dtype=torch.int32, device=seq_lens.device)
     row_len = row_len if row_len is not None else torch.empty(rows, dtype=torch.int32, device=seq_lens.device)
-    _check("bsp_row_lengths_decode", lib().bsp_row_lengths_decode(_ptr(seq_lens), seq_lens.numel(), q_len, num_heads,
+    _check("bsp_row_lengths_decode", lib().bsp_row_lengths_decode(_io_ptr(seq_lens), seq_lens.numel(), q_len, num_heads,
                                                                   _ptr(row_seq), _ptr(row_len), _stream(stream)))
     return row_seq, row_len
 
@@ -273,8 +285,8 @@ def sparse_pa_decode(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, k_pages
     if ws is None:
         ws = decode_workspace(rows, k_pages, num_q_heads // kv.num_kv_heads, q.device)
     _check("bsp_sparse_pa_decode",
-           lib().bsp_sparse_pa_decode(C.byref(kv.desc), _ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
-                                      _ptr(sparse_ctx), rows, k_pages, sm_scale, _ptr(out), _ptr(ws), ws.numel(),
+           lib().bsp_sparse_pa_decode(C.byref(kv.desc), _io_ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
+                                      _ptr(sparse_ctx), rows, k_pages, sm_scale, _io_ptr(out), _ptr(ws), ws.numel(),
                                       _ptr(dev_err), _stream(stream)))
     return out
 
@@ -287,8 +299,8 @@ def sparse_pa_decode_noalloc(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx,
     sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(128)
     out = out if out is not None else torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     _check("bsp_sparse_pa_decode_noalloc",
-           lib().bsp_sparse_pa_decode_noalloc(C.byref(kv.desc), _ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
-                                              _ptr(sparse_ctx), rows, k_pages, sm_scale, _ptr(out), _ptr(dev_err),
+           lib().bsp_sparse_pa_decode_noalloc(C.byref(kv.desc), _io_ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
+                                              _ptr(sparse_ctx), rows, k_pages, sm_scale, _io_ptr(out), _ptr(dev_err),
                                               _stream(stream)))
     return out
 
@@ -299,8 +311,8 @@ def sparse_pa_prefill(kv, q, q_dtype, num_q_heads, sparse_bt, sparse_ctx, k_page
     sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(128)
     out = out if out is not None else torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     _check("bsp_sparse_pa_prefill",
-           lib().bsp_sparse_pa_prefill(C.byref(kv.desc), _ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
-                                       _ptr(sparse_ctx), rows, k_pages, sm_scale, _ptr(out), _ptr(dev_err),
+           lib().bsp_sparse_pa_prefill(C.byref(kv.desc), _io_ptr(q), q_dtype, num_q_heads, _ptr(sparse_bt),
+                                       _ptr(sparse_ctx), rows, k_pages, sm_scale, _io_ptr(out), _ptr(dev_err),
                                        _stream(stream)))
     return out
 

@@ -74,11 +74,14 @@ def test_host_validation_without_a_gpu():
 
 
 def test_binding_refuses_pageable_host_tensors():
-    """Tensors reach the library as device addresses: CUDA tensors, or pinned
-    host tensors (mapped into the device's address space).  A pageable host
-    tensor has no device address and is refused before any call."""
+    """Tensors reach the library as device addresses: CUDA tensors, or, for
+    the per-token inputs and outputs only, pinned host tensors (mapped into
+    the device's address space).  A pageable host tensor has no device
+    address and is refused before any call, in either role."""
     import torch
     from block_sparse_paged_score_gb300 import bsp
-    assert bsp._ptr(None) is None
+    assert bsp._ptr(None) is None and bsp._io_ptr(None) is None
     with pytest.raises(ValueError):
         bsp._ptr(torch.empty(4))
+    with pytest.raises(ValueError):
+        bsp._io_ptr(torch.empty(4))

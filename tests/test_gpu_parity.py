@@ -421,6 +421,15 @@ def test_host_argument_errors(bsp):
         bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb128).cuda(), torch.from_numpy(ctx).cuda(),
                              128, ws=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.status == 3
+    # pinned host memory is refused, before any call, where the kernels need
+    # device memory (selections, score rows); it is taken only for per-token
+    # inputs and outputs
+    with pytest.raises(ValueError):
+        bsp.sparse_pa_decode(g.kv, g.q, w.q_dtype, w.hq, torch.from_numpy(sb).pin_memory(),
+                             torch.from_numpy(ctx).cuda(), w.k_pages)
+    with pytest.raises(ValueError):
+        bsp.topk_select(torch.from_numpy(np.ascontiguousarray(o.scores(), np.float32)).pin_memory(), rs, rl,
+                        g.block_table, w.kv_dtype, w.k_pages)
 
 
 @pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx"])
