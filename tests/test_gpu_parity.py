@@ -127,16 +127,21 @@ def test_topk_bit_exact_on_oracle_scores(bsp, name):
     assert np.array_equal(gctx.cpu().numpy(), ctx)
 
 
-@pytest.mark.parametrize("max_pages", [100, 256, 700, 701, 2047, 2048, 3000, 8000, 9000])
+@pytest.mark.parametrize("max_pages", [100, 256, 700, 701, 2047, 2048, 3000, 8000, 9000, 12000, 40000, 65536])
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
 def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
-    """All three selectors: one warp per row up to 128 pages, one CTA with
-    the keys in registers up to 8192, one CTA with the keys in shared memory
-    beyond.  Widths that are not a multiple of 4 pages (701, 2047) take the
-    CTA kernel's one-key-at-a-time score loads instead of its 16-byte ones."""
+    """Every selector: one warp per row up to 128 pages; one CTA with the
+    keys in registers up to 8192 (256 threads, or 512/1024 threads when there
+    are fewer rows than twice the SMs, up to 32768: the 8000 and 9000 cases);
+    beyond that one 512-thread CTA with the keys in shared memory up to 16384
+    candidates (12000 pages over 320 rows) or read from global memory (rows
+    of 40000 and 65536 pages, the largest width).  Widths that are not a
+    multiple of 4 pages (701, 2047) take the CTA kernel's one-key-at-a-time
+    score loads instead of its 16-byte ones.  k runs up to 2048 pages, the
+    largest the call takes."""
     rng = np.random.default_rng(3)
-    rows = 300 if max_pages <= 4096 else 60
+    rows = 300 if max_pages <= 4096 else 60 if max_pages <= 9000 else 320 if max_pages <= 16384 else 20
     sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
     sc[::5] = rng.standard_normal((len(sc[::5]), max_pages)).astype(np.float32)
     sc[7, ::3] = -0.0
@@ -146,7 +151,7 @@ def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
     nblk = (max_pages + 7) // 8
     bt = np.stack([rng.permutation(4 * nblk)[:nblk] for _ in range(rows)]).astype(np.int32)
     rs = np.arange(rows, dtype=np.int32)
-    for k in (1, 2, 37, 128):
+    for k in (1, 2, 37, 128, 2048):
         ti, sb, ctx = O.topk_select(sc, rs, L, bt, 1 if kv_dtype == W.MXFP4 else 0, k, force_tail)
         gti, gsb, gctx = bsp.topk_select(torch.from_numpy(sc).cuda(), torch.from_numpy(rs).cuda(),
                                          torch.from_numpy(L).cuda(), torch.from_numpy(bt).cuda(), kv_dtype, k,
