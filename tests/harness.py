@@ -38,9 +38,20 @@ MINI = {
                   prefill_chunks=[(384, 200), (700, 300)], pad_seqs=1, pad_q_len=4),
 }
 
+# longer decode contexts, one per width of the scorer's fused selection
+# (rows up to 128 * w pages for w = 8, 16 and 32 keys per thread)
+LONG = {
+    "fp8_long8": dict(name="long-fp8-1000p", seed=21, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16,
+                      idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=128, q_len=2, decode_lens=[9000, 16000]),
+    "fp8_long16": dict(name="long-fp8-1875p", seed=22, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16,
+                       idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=128, q_len=2, decode_lens=[2100, 30000]),
+    "fp8_long32": dict(name="long-fp8-4096p", seed=23, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16,
+                       idx_q_dtype=W.FP8, hkv=1, group=16, k_pages=128, q_len=2, decode_lens=[40000, 65536]),
+}
+
 
 def mini(name):
-    return W.Workload(MINI[name])
+    return W.Workload(MINI[name] if name in MINI else LONG[name])
 
 
 class OracleSide:

@@ -29,8 +29,10 @@ def run_gpu(bsp, sc, rs, L, bt, kv_dtype, k, force_tail):
     return gti.cpu().numpy(), gsb.cpu().numpy(), gctx.cpu().numpy()
 
 
-# blocks per row 13 .. 8192: every blocks-per-thread variant (1 .. 32)
-@pytest.mark.parametrize("max_pages", [100, 2048, 4000, 8000, 16000, 40000, 65536])
+# blocks per row 13 .. 8192: every blocks-per-thread variant (1, 2, 4, 8, 16
+# and 32 blocks a thread at 256 threads: 13-256, 500, 1000, 2000, 3750, 5000
+# and 8192 blocks)
+@pytest.mark.parametrize("max_pages", [100, 2048, 4000, 8000, 16000, 30000, 40000, 65536])
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
 def test_block_select_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):

@@ -127,21 +127,30 @@ def test_topk_bit_exact_on_oracle_scores(bsp, name):
     assert np.array_equal(gctx.cpu().numpy(), ctx)
 
 
-@pytest.mark.parametrize("max_pages", [100, 256, 700, 701, 2047, 2048, 3000, 8000, 9000, 12000, 40000, 65536])
+# (width in pages, row count): "many" rows (at least twice the SMs) take the
+# 256-thread CTA selector, "few" the 512/1024-thread one, "long" rows past
+# 32768 pages the long-row kernel
+TIE_CASES = [(100, "many"), (256, "many"), (500, "many"), (1000, "many"), (2047, "many"), (2048, "many"),
+             (3000, "many"), (6000, "many"), (12000, "many"), (300, "few"), (700, "few"), (701, "few"),
+             (4000, "few"), (8000, "few"), (9000, "few"), (20000, "few"), (40000, "long"), (65536, "long")]
+
+
+@pytest.mark.parametrize("max_pages,regime", TIE_CASES)
 @pytest.mark.parametrize("force_tail", [True, False])
 @pytest.mark.parametrize("kv_dtype", [W.FP8, W.MXFP4])
-def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages):
-    """Every selector: one warp per row up to 128 pages; one CTA with the
-    keys in registers up to 8192 (256 threads, or 512/1024 threads when there
-    are fewer rows than twice the SMs, up to 32768: the 8000 and 9000 cases);
-    beyond that one 512-thread CTA with the keys in shared memory up to 16384
-    candidates (12000 pages over 320 rows) or read from global memory (rows
-    of 40000 and 65536 pages, the largest width).  Widths that are not a
-    multiple of 4 pages (701, 2047) take the CTA kernel's one-key-at-a-time
-    score loads instead of its 16-byte ones.  k runs up to 2048 pages, the
-    largest the call takes."""
+def test_topk_bit_exact_with_ties(bsp, force_tail, kv_dtype, max_pages, regime):
+    """Every selector shape: one warp per row up to 128 pages; with many rows
+    one 256-thread CTA with 1 to 32 keys per thread in registers up to 8192
+    pages (256 ... 6000), then the long-row kernel with the keys in shared
+    memory (12000); with fewer rows than twice the SMs one 512- or
+    1024-thread CTA up to 32768 pages (300 ... 20000); rows past that read
+    their keys from global memory (40000, and 65536, the largest width).
+    Widths that are not a multiple of 4 pages (701, 2047) take the CTA
+    kernel's one-key-at-a-time score loads instead of its 16-byte ones.  k
+    runs up to 2048 pages, the largest the call takes."""
     rng = np.random.default_rng(3)
-    rows = 300 if max_pages <= 4096 else 60 if max_pages <= 9000 else 320 if max_pages <= 16384 else 20
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = {"many": 2 * sms + 16, "few": 60, "long": 20}[regime]
     sc = rng.integers(-4, 5, (rows, max_pages)).astype(np.float32)  # heavy ties
     sc[::5] = rng.standard_normal((len(sc[::5]), max_pages)).astype(np.float32)
     sc[7, ::3] = -0.0
@@ -485,10 +494,11 @@ def test_mixed_step_zero_copy_matches_device_step(bsp):
             assert torch.equal(out, ref.cpu()), (inputs, output)
 
 
-@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2"])
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "fp8_long8", "fp8_long16", "fp8_long32"])
 def test_decode_step_selection_in_scorer(bsp, name):
     """With sel_counters the scorer's last CTA of each sequence selects its
-    rows.  On two steps in a row (the counters are left at zero): its tables
+    rows, with 4, 8, 16 or 32 keys per thread by the width of the rows (the
+    two short workloads, then rows of 1000, 1875 and 4096 pages).  On two steps in a row (the counters are left at zero): its tables
     equal, bit for bit, the oracle's top-k run on the step's own score rows;
     the score rows are within the score bound of the oracle's; the output is
     within the attention tolerance of the oracle's attention on the step's
