@@ -12,7 +12,8 @@ cache, with full, ragged and empty contexts, so the oracle's attention over
 700 rows stays cheap.  Each call is compared with the oracle's attention on
 the same cache bytes, queries and tables, within the attention tolerance.
 One workspace serves every call, so each call must leave its arrival
-counters at zero for the next.
+counters at zero for the next.  Where the plan gives each row one CTA, the
+decode call must equal the plan-free prefill call bit for bit.
 """
 import numpy as np
 import pytest
@@ -84,6 +85,14 @@ def test_attention_for_any_row_count(name):
         assert err.item() == 0, n
         ok, worst, rl2 = attention_close(bf16_f32(out).reshape(n, w.group, 128), ref[:n], label=f"{name} rows={n}")
         assert ok, (n, worst, rl2)
-        splits.add(bsp.decode_splits(w.kv_dtype, n, K_PAGES))
+        ns = bsp.decode_splits(w.kv_dtype, n, K_PAGES)
+        splits.add(ns)
+        if ns == 1:
+            # one CTA a row: the planned decode call equals the plan-free
+            # prefill call bit for bit
+            pre = bsp.sparse_pa_prefill(kv, q_dev[:n], w.q_dtype, hq, sb_dev[:n], ctx_dev[:n], K_PAGES, SM_SCALE,
+                                        dev_err=err)
+            torch.cuda.synchronize()
+            assert err.item() == 0 and torch.equal(pre, out), n
     # the sweep reached all three ways of finishing a row
     assert 1 in splits and any(2 <= s <= 8 for s in splits) and any(s > 8 for s in splits), sorted(splits)
