@@ -128,17 +128,17 @@ def kernel_sources(files):
     """The kernel's sources and every local header they include, directly or
     through another header (`#include "..."`), as sorted repository paths."""
     csrc = os.path.join(ROOT, "block_sparse_paged_score_gb300", "csrc")
-    todo = [os.path.normpath(os.path.join(csrc, f)) for f in files]
+    pending = [os.path.normpath(os.path.join(csrc, f)) for f in files]
     seen = set()
-    while todo:
-        f = todo.pop()
+    while pending:
+        f = pending.pop()
         if f in seen:
             continue
         seen.add(f)
         for line in open(f):
             m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
             if m:
-                todo.append(os.path.normpath(os.path.join(os.path.dirname(f), m.group(1))))
+                pending.append(os.path.normpath(os.path.join(os.path.dirname(f), m.group(1))))
     return sorted(os.path.relpath(f, ROOT) for f in seen)
 
 
