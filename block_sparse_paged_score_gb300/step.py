@@ -8,8 +8,11 @@ scores, top-k with the emitted sparse table, split-K attention and merge --
 on one stream, without host synchronisation.
 
 ``HostDecodeStep`` is the end-to-end form a serving loop uses: the step's
-inputs arrive in pinned host memory, are copied to the device, the step runs,
-and the attention output is copied back.
+inputs arrive in pinned host memory and its attention output must land
+there.  Each direction either crosses by one copy-engine copy or is read or
+written in place by the step's kernels (zero-copy).  ``MixedStep`` is the
+chunked-prefill batch (decode rows first, then prefill chunks and pad rows)
+as separate calls on one stream.
 """
 import ctypes as C
 
