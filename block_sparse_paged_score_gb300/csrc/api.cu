@@ -183,12 +183,12 @@ bsp_status bsp_row_lengths_prefill(const int32_t* query_req_id, const int32_t* q
   return st;
 }
 
-// seq_is_group: the decode step's own rows, where query group g is sequence g
-static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
-                                   const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
-                                   const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
-                                   float* scores, int32_t* dev_err, bsp_stream_t stream, int32_t seq_is_group,
-                                   const TopkParams* sel = nullptr, int32_t* sel_counters = nullptr) {
+// the decode scorer's argument checks (also run by the decode step before its
+// first launch)
+static bsp_status index_score_check(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
+                                    const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
+                                    const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
+                                    const float* scores) {
   bsp_status st = check_idx(idx);
   if (st != BSP_OK) return st;
   if (num_rows < 0 || max_pages < 1 || bt_stride < 1) return BSP_ERR_INVALID_ARG;
@@ -198,6 +198,18 @@ static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q
   if (static_cast<int64_t>(max_pages) > static_cast<int64_t>(bt_stride) * 8) return BSP_ERR_INVALID_ARG;
   if (num_rows == 0) return BSP_OK;
   if (!idx_q || !block_table || !row_seq || !row_len || !scores || !al(idx_q, 8)) return BSP_ERR_INVALID_ARG;
+  return BSP_OK;
+}
+
+// seq_is_group: the decode step's own rows, where query group g is sequence g
+static bsp_status index_score_impl(const bsp_index_cache* idx, const void* idx_q, int32_t q_dtype,
+                                   const int32_t* block_table, int32_t bt_stride, const int32_t* row_seq,
+                                   const int32_t* row_len, int32_t num_rows, int32_t q_group, int32_t max_pages,
+                                   float* scores, int32_t* dev_err, bsp_stream_t stream, int32_t seq_is_group,
+                                   const TopkParams* sel = nullptr, int32_t* sel_counters = nullptr) {
+  bsp_status st = index_score_check(idx, idx_q, q_dtype, block_table, bt_stride, row_seq, row_len, num_rows,
+                                    q_group, max_pages, scores);
+  if (st != BSP_OK || num_rows == 0) return st;
   IndexScoreParams p{};
   p.idx_dtype = idx->dtype;
   p.hidx = idx->num_heads;
@@ -420,6 +432,15 @@ static bsp_status sparse_pa_common(const bsp_kv_cache* kv, const void* q, int32_
   return st;
 }
 
+// the decode attention's workspace check (also run by the decode step before
+// its first launch): a plan that merges through the workspace needs `need`
+// bytes of it, 16-byte aligned
+static bsp_status sparse_pa_ws_check(int32_t kv_dtype, int32_t num_rows, int32_t k_pages, const void* ws,
+                                     size_t ws_bytes) {
+  const size_t need = sparse_pa_decode_ws_need(kv_dtype, num_rows, k_pages);
+  return need && (!ws || ws_bytes < need || !al(ws, 16)) ? BSP_ERR_WORKSPACE : BSP_OK;
+}
+
 bsp_status bsp_sparse_pa_decode(const bsp_kv_cache* kv, const void* q, int32_t q_dtype, int32_t num_q_heads,
                                 const int32_t* sparse_bt, const int32_t* sparse_ctx, int32_t num_rows,
                                 int32_t k_pages, float sm_scale, void* out, void* ws, size_t ws_bytes,
@@ -460,10 +481,37 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   if (reuse ? (!a->sparse_bt || !a->sparse_ctx)
             : (!a->idx_q || !al(a->idx_q, 16) || !a->seq_lens || !a->row_seq || !a->row_len))
     return BSP_ERR_INVALID_ARG;
+  const bool cast_q = a->q_dtype == BSP_FP8_E4M3, cast_iq = !reuse && a->idx_q_dtype == BSP_FP8_E4M3;
+  if ((cast_q && (!a->q_cast || !al(a->q_cast, 16))) || (cast_iq && (!a->idx_q_cast || !al(a->idx_q_cast, 16))))
+    return BSP_ERR_INVALID_ARG;
+  // the queries the scorer and the attention read
+  const void* q = cast_q ? a->q_cast : a->q;
+  const void* iq = cast_iq ? a->idx_q_cast : a->idx_q;
+  // The step's rows are decode-ordered (row_seq = token / q_len, as the prep
+  // kernel writes it): the scorer and the selector find a row's sequence
+  // without reading row_seq first.  With sel_counters the scorer's last CTA
+  // of each query group selects the group's rows (no selector launch).
+  const int32_t topk_flags = a->flags & (BSP_FORCE_TAIL | BSP_SELECT_BLOCKS);
+  const bool fused = !reuse && a->sel_counters &&
+                     index_score_can_select(a->idx->dtype, a->idx_q_dtype, a->max_pages,
+                                            (a->flags & BSP_SELECT_BLOCKS) != 0);
+  // every later stage's checks too, so that an invalid step enqueues nothing
+  TopkParams sel;
+  if (!reuse) {
+    if (fused && !al(a->sel_counters, 4)) return BSP_ERR_INVALID_ARG;
+    if ((st = index_score_check(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len,
+                                rows, a->q_len, a->max_pages, a->scores)) != BSP_OK ||
+        (st = topk_params(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
+                          a->kv->dtype, a->k_pages, topk_flags, a->topk_idx, a->sparse_bt, a->sparse_ctx,
+                          a->q_len * hkv, sel)) != BSP_OK)
+      return st;
+  }
+  if ((st = sparse_pa_check_args(a->kv, q, a->q_dtype, a->num_q_heads, a->sparse_bt, a->sparse_ctx, rows, a->k_pages,
+                                 a->out)) != BSP_OK ||
+      (st = sparse_pa_ws_check(a->kv->dtype, rows, a->k_pages, a->ws, a->ws_bytes)) != BSP_OK)
+    return st;
   mark(0);
   // write + e4m3 casts + row lengths: one launch
-  const void* q = a->q;
-  const void* iq = a->idx_q;
   DecodePrepParams pp{};
   KvWriteParams& w = pp.write;
   w.kv_dtype = a->kv->dtype;
@@ -487,19 +535,15 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   w.slot = a->slot;
   w.num_tokens = a->num_new_tokens;
   w.err = a->dev_err;
-  if (a->q_dtype == BSP_FP8_E4M3) {
-    if (!a->q_cast || !al(a->q_cast, 16)) return BSP_ERR_INVALID_ARG;
+  if (cast_q) {
     pp.cast_src[0] = static_cast<const uint16_t*>(a->q);
     pp.cast_dst[0] = static_cast<uint8_t*>(a->q_cast);
     pp.cast_n[0] = static_cast<int64_t>(tokens) * a->num_q_heads * kDim;
-    q = a->q_cast;
   }
-  if (!reuse && a->idx_q_dtype == BSP_FP8_E4M3) {
-    if (!a->idx_q_cast || !al(a->idx_q_cast, 16)) return BSP_ERR_INVALID_ARG;
+  if (cast_iq) {
     pp.cast_src[1] = static_cast<const uint16_t*>(a->idx_q);
     pp.cast_dst[1] = static_cast<uint8_t*>(a->idx_q_cast);
     pp.cast_n[1] = static_cast<int64_t>(tokens) * hidx * kDim;
-    iq = a->idx_q_cast;
   }
   if (!reuse) {  // the selection's rows; nothing to compute when it is reused
     pp.seq_lens = a->seq_lens;
@@ -512,22 +556,6 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   if ((st = cuda_status(launch_decode_prep(pp, s))) != BSP_OK) return st;
   ++g_launches;
   mark(1);
-  // the step's rows are decode-ordered (row_seq = token / q_len, as the prep
-  // kernel writes it): the scorer and the selector find a row's sequence
-  // without reading row_seq first.  With sel_counters the scorer's last CTA
-  // of each query group selects the group's rows (no selector launch).
-  const int32_t topk_flags = a->flags & (BSP_FORCE_TAIL | BSP_SELECT_BLOCKS);
-  const bool fused = !reuse && a->sel_counters &&
-                     index_score_can_select(a->idx->dtype, a->idx_q_dtype, a->max_pages,
-                                            (a->flags & BSP_SELECT_BLOCKS) != 0);
-  TopkParams sel;
-  if (fused) {
-    if (!al(a->sel_counters, 4)) return BSP_ERR_INVALID_ARG;
-    if ((st = topk_params(a->scores, rows, a->max_pages, a->row_seq, a->row_len, a->block_table, a->bt_stride,
-                          a->kv->dtype, a->k_pages, topk_flags, a->topk_idx, a->sparse_bt, a->sparse_ctx,
-                          a->q_len * hkv, sel)) != BSP_OK)
-      return st;
-  }
   if (!reuse &&
       (st = index_score_impl(a->idx, iq, a->idx_q_dtype, a->block_table, a->bt_stride, a->row_seq, a->row_len, rows,
                              a->q_len, a->max_pages, a->scores, a->dev_err, stream, 1, fused ? &sel : nullptr,

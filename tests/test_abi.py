@@ -85,3 +85,52 @@ def test_binding_refuses_pageable_host_tensors():
         bsp._ptr(torch.empty(4))
     with pytest.raises(ValueError):
         bsp._io_ptr(torch.empty(4))
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device addresses must never reach a GPU")
+def test_invalid_decode_step_enqueues_nothing():
+    """bsp_sparse_decode_step checks every stage's arguments (scorer,
+    selector, attention and its workspace) before its first event or launch:
+    an invalid step returns its status with nothing enqueued.  Without a GPU
+    any launch would fail with BSP_ERR_CUDA, so each documented status below
+    shows that the call returned before its first launch."""
+    from block_sparse_paged_score_gb300 import bsp
+    L = bsp.lib()
+    fake = 1 << 20  # host-side descriptors and addresses only; never dereferenced
+    kv, ic = bsp.KvCacheDesc(), bsp.IndexCacheDesc()
+    assert L.bsp_kv_cache_interleaved(bsp.FP8_E4M3, 1, fake, 64, 0.5, 0.5, C.byref(kv)) == 0
+    assert L.bsp_index_cache_packed(bsp.FP8_E4M3, 1, fake, 64, C.byref(ic)) == 0
+
+    def args(**kw):
+        a = bsp.DecodeStepArgs()
+        a.kv, a.idx = C.pointer(kv), C.pointer(ic)
+        for f in ("k_new", "v_new", "idx_k_new", "slot", "q", "q_cast", "idx_q", "idx_q_cast", "seq_lens",
+                  "block_table", "row_seq", "row_len", "scores", "topk_idx", "sparse_bt", "sparse_ctx", "out", "ws",
+                  "dev_err"):
+            setattr(a, f, fake)
+        a.num_new_tokens, a.num_seqs, a.q_len, a.num_q_heads = 1, 1, 1, 16
+        a.q_dtype, a.idx_q_dtype = bsp.BF16, bsp.FP8_E4M3
+        a.bt_stride, a.max_pages, a.k_pages, a.flags, a.sm_scale = 8, 64, 16, bsp.FORCE_TAIL, 0.088
+        a.ws_bytes, a.sel_counters = 1 << 30, None
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    cases = [
+        (dict(num_q_heads=3), 2),                   # 3 query heads per KV head (attention)
+        (dict(k_pages=4096), 2),                    # more pages than the selector takes
+        (dict(max_pages=100), 1),                   # wider than the block table covers (scorer)
+        (dict(k_pages=2048, ws_bytes=16), 3),       # one row split 64 ways needs a workspace
+        (dict(out=None), 1),                        # no output (attention)
+        (dict(scores=None), 1),                     # no score rows (scorer)
+        (dict(topk_idx=None), 1),                   # no selection output (selector)
+        (dict(sel_counters=fake + 2), 1),           # misaligned counters (fused selection)
+        (dict(idx_q_cast=None), 1),                 # e4m3 index queries need their cast buffer
+        (dict(q_dtype=bsp.FP8_E4M3, q_cast=None), 1),
+        (dict(flags=bsp.FORCE_TAIL | bsp.REUSE_SELECTION, num_q_heads=3), 2),
+    ]
+    n0 = L.bsp_launch_count()
+    for kw, want in cases:
+        assert L.bsp_sparse_decode_step(C.byref(args(**kw)), None, None) == want, kw
+    assert L.bsp_launch_count() == n0
