@@ -464,6 +464,7 @@ bsp_status bsp_sparse_decode_step(const bsp_decode_step_args* a, bsp_event_t* ev
   const int32_t hidx = reuse ? 0 : a->idx->num_heads;
   if (!reuse && hidx != hkv) return BSP_ERR_UNSUPPORTED;  // rows are shared by the scorer and the attention
   if (a->num_seqs < 0 || a->q_len < 1 || a->q_len > 8) return BSP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(a->num_seqs) * a->q_len * hkv > INT32_MAX) return BSP_ERR_UNSUPPORTED;  // int32 rows
   const int32_t tokens = a->num_seqs * a->q_len;
   const int32_t rows = tokens * hkv;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -129,6 +129,7 @@ def test_invalid_decode_step_enqueues_nothing():
         (dict(idx_q_cast=None), 1),                 # e4m3 index queries need their cast buffer
         (dict(q_dtype=bsp.FP8_E4M3, q_cast=None), 1),
         (dict(flags=bsp.FORCE_TAIL | bsp.REUSE_SELECTION, num_q_heads=3), 2),
+        (dict(num_seqs=1 << 29, q_len=8), 2),     # more rows than an int32 counts
     ]
     n0 = L.bsp_launch_count()
     for kw, want in cases:
