@@ -33,6 +33,11 @@ MINI = {
     # two KV / index heads with the tcgen05 MXFP4 scorer (e4m3 index queries)
     "mx_h2": dict(name="mini-mx-h2", seed=20, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8, idx_q_dtype=W.FP8,
                   hkv=2, group=8, k_pages=16, q_len=2, decode_lens=[7, 129, 900, 2000]),
+    # four KV / index heads per GPU (the deployment without tensor parallelism)
+    "fp8_h4": dict(name="mini-fp8-h4", seed=40, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
+                   hkv=4, group=16, k_pages=16, q_len=2, decode_lens=[3, 200, 1300]),
+    "mx_h4": dict(name="mini-mx-h4", seed=41, kv_dtype=W.MXFP4, idx_dtype=W.MXFP4, q_dtype=W.FP8, idx_q_dtype=W.FP8,
+                  hkv=4, group=16, k_pages=16, q_len=2, decode_lens=[5, 260, 1100]),
     "mixed": dict(name="mini-mixed", seed=17, kv_dtype=W.FP8, idx_dtype=W.FP8, q_dtype=W.BF16, idx_q_dtype=W.FP8,
                   hkv=1, group=16, k_pages=16, q_len=1, decode_lens=[40, 900],
                   prefill_chunks=[(384, 200), (700, 300)], pad_seqs=1, pad_q_len=4),

@@ -255,7 +255,7 @@ def test_attention_large_batches(bsp, name):
             assert int(counters.abs().sum().item()) == 0
 
 
-@pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx"])
+@pytest.mark.parametrize("name", ["bf16", "fp8", "fp8_q4_h2", "mx", "fp8_h4", "mx_h4"])
 def test_pipeline_end_to_end(bsp, name):
     """GPU path and oracle path run independently from the same inputs."""
     w, o, g = sides(name)
@@ -283,7 +283,7 @@ def test_pipeline_end_to_end(bsp, name):
     print(f"{name}: {int((~same).sum())} rows with near-tie swaps; worst err/allowed {mx:.3g} rel-L2 {rl2:.3g}")
 
 
-@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx", "bf16"])
+@pytest.mark.parametrize("name", ["fp8", "fp8_q4_h2", "mx", "bf16", "fp8_h4", "mx_h4"])
 def test_decode_step_matches_ops(bsp, name):
     """bsp_sparse_decode_step == the separate calls, bit for bit."""
     from block_sparse_paged_score_gb300 import step
